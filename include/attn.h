@@ -1,0 +1,159 @@
+/*
+ * attn.h -- C ABI of libattn.so: exact attention forward with online softmax
+ * on NVIDIA GB300 (sm_103a).
+ *
+ * The operation (all three source pages compute it; they differ only in how
+ * they tile it):
+ *
+ *   O[b,h,i,:] = sum_j softmax_j( scale * Q[b,h,i,:] . K[b,h,j,:] ) * V[b,h,j,:]
+ *
+ * over the keys j visible to query i, computed tile by tile: each query row
+ * keeps a running maximum m, a normaliser l and an unnormalised accumulator a,
+ * and both l and a are multiplied by exp(m_old - m_new) whenever a new key
+ * tile raises the maximum, so that the full score matrix is never formed.
+ *   - definition and dense reference: aiml.sh "verify-tiled-attention",
+ *     function standard_attention (scale 1/sqrt(d), causal limit i+1);
+ *     deepnotes "flash-attention-implemented-verified-and-measured",
+ *     naive_attention on [B, H, S, d] tensors;
+ *   - the tiled recurrence: aiml.sh "verify-tiled-attention",
+ *     tiled_flash_attention; deepnotes ..., tiled_attention_online_softmax;
+ *     huhohoo "tiled-online-softmax", section "Online normalization".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout   q [B, H, Sq, d], k and v [B, H, Skv, d], o [B, H, Sq, d],
+ *          lse [B, H, Sq]; all contiguous row-major, strides implied.
+ *          q, k, v and o must be 16-byte aligned; lse 4-byte aligned.
+ * causal   0 or 1.  Key j is visible to query i iff j <= i + (Skv - Sq)
+ *          (bottom-right alignment; identical to the pages' j <= i when
+ *          Sq == Skv).  A query row with no visible key gets o = 0 and
+ *          lse = -inf.
+ * scale    multiplies q . k.  scale <= 0 selects the pages' 1/sqrt(d); NaN or
+ *          infinity is rejected.
+ * lse      optional (NULL: not written).  Natural-log log-sum-exp of the
+ *          scaled scores of each row, fp32.  Not on the pages; provided so a
+ *          caller can merge partial results or compute a backward pass.
+ * stream   a cudaStream_t (NULL = legacy default stream).  All work is
+ *          enqueued on it asynchronously; no entry point synchronises except
+ *          attn_check_status.  Device pointers must be valid on the current
+ *          CUDA device.
+ * Ownership  the caller owns every buffer.  The library keeps no per-call
+ *          allocation; q, k and v are only read; o and lse must not overlap
+ *          q, k or v (rejected) or each other.
+ * Empty    B, H or Sq equal to 0 is a no-op returning ATTN_OK; Skv == 0 writes
+ *          o = 0 and lse = -inf.
+ * Errors   every entry point returns an attn_status; nothing aborts, exits or
+ *          traps.  Invalid arguments are detected on the host before any
+ *          launch.  attn_strerror() gives a message.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_ABI_VERSION 1
+
+typedef enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,        /* null/misaligned/overlapping pointer, bad size or dtype */
+    ATTN_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not compute capability 10.3 */
+    ATTN_ERR_LAUNCH = 3,             /* a CUDA launch or copy failed */
+    ATTN_ERR_TIMEOUT = 4,            /* a kernel's bounded wait expired (see attn_check_status) */
+    ATTN_ERR_CUDA = 5                /* another CUDA runtime/driver error */
+} attn_status;
+
+typedef enum attn_dtype {
+    ATTN_F32 = 0,          /* fp32 q/k/v/o; CUDA-core kernel, fp32 arithmetic */
+    ATTN_BF16 = 1,         /* bf16 q/k/v/o; tensor-core kernel, fp32 accumulation */
+    ATTN_F16 = 2,          /* fp16 q/k/v/o; tensor-core kernel, fp32 accumulation */
+    ATTN_BF16_OUT_F32 = 3, /* bf16 q/k/v, fp32 o (no output rounding) */
+    ATTN_F16_OUT_F32 = 4   /* fp16 q/k/v, fp32 o */
+} attn_dtype;
+
+/*
+ * attn_fwd -- exact attention forward (the operation above).
+ *
+ * Supported head widths: ATTN_F32: d in {16, 32, 64, 128};
+ * ATTN_BF16/F16 and their _OUT_F32 variants: d in {64, 128}.
+ * ATTN_F32 runs the CUDA-core kernel with 32-row query blocks and 64-key
+ * blocks (the key block of deepnotes "Correctness first"); the 16-bit types
+ * run the tensor-core kernel with 128 x 128 tiles.
+ * Requires a compute capability 10.3 device (GB300) for every dtype.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int H, int Sq, int Skv, int d, int causal, float scale,
+             int dtype, void *stream);
+
+/*
+ * attn_validate -- the host-side argument check of attn_fwd, without any CUDA
+ * call or launch.  Returns ATTN_OK or ATTN_ERR_INVALID_ARG.  Pointers are only
+ * compared and tested for alignment, never dereferenced.
+ */
+int attn_validate(const void *q, const void *k, const void *v, const void *o,
+                  const float *lse, int B, int H, int Sq, int Skv, int d,
+                  int causal, float scale, int dtype);
+
+/*
+ * attn_fwd_f32_blocked -- the fp32 CUDA-core path with caller-chosen tile
+ * sizes, so that block-size invariance (including sizes that do not divide
+ * the sequence, e.g. 7, or 13 x 19) can be tested as the pages do
+ * (aiml.sh "verify-tiled-attention" test_lab.py tile sweep; huhohoo
+ * "tiled-online-softmax" exercise with block size seven).
+ * block_q in [1, 128], block_kv in [1, 256]; the key tile must fit in shared
+ * memory (ATTN_ERR_INVALID_ARG otherwise).  Other arguments as attn_fwd with
+ * dtype ATTN_F32.
+ */
+int attn_fwd_f32_blocked(const float *q, const float *k, const float *v,
+                         float *o, float *lse, int B, int H, int Sq, int Skv,
+                         int d, int causal, float scale, int block_q,
+                         int block_kv, void *stream);
+
+/*
+ * attn_fwd_staged -- attn_fwd on HOST buffers: copies q, k, v from host memory
+ * to the caller's device buffers dq, dk, dv, runs attn_fwd into do_ / dlse,
+ * and copies o (and lse when both lse_host and dlse are non-NULL) back to
+ * host memory, all enqueued on `stream` (one cudaMemcpyAsync per tensor).
+ * Host buffers should be pinned for the copies to be asynchronous.  The call
+ * returns after enqueueing; synchronise the stream before reading o_host.
+ * Sizes and dtype as attn_fwd; host pointers must not be NULL when their
+ * tensor is non-empty.
+ */
+int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
+                    void *o_host, float *lse_host, void *dq, void *dk, void *dv,
+                    void *do_, float *dlse, int B, int H, int Sq, int Skv,
+                    int d, int causal, float scale, int dtype, void *stream);
+
+/*
+ * attn_check_status -- synchronises `stream`, then reads and clears the
+ * library's device status word on the current device.  Returns
+ * ATTN_ERR_TIMEOUT if any tensor-core kernel since the last check gave up a
+ * bounded wait (its output is then incomplete), ATTN_ERR_CUDA if the stream
+ * reports an error, ATTN_OK otherwise.
+ */
+int attn_check_status(void *stream);
+
+/* Human-readable text for an attn_status value (static storage). */
+const char *attn_strerror(int status);
+
+/* ATTN_ABI_VERSION of the loaded library. */
+int attn_abi_version(void);
+
+/*
+ * Test hook for the watchdog of the tensor-core kernel.  hook = 0 (default)
+ * disables it; hook = 1 makes the next launches skip one internal
+ * completion signal, so that a bounded wait expires, the kernel stops
+ * cleanly and attn_check_status reports ATTN_ERR_TIMEOUT.  timeout_ns sets
+ * the bounded-wait limit (0 keeps the current value; default 1e9 ns).
+ * Process-wide; not thread-safe against concurrent attn_fwd calls.
+ */
+int attn_test_set_hook(int hook, uint64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

@@ -1,0 +1,227 @@
+"""Python binding of libattn.so -- exact attention forward with online softmax
+for GB300 (sm_103a).
+
+The functions named like the C ABI (``attn_fwd``, ``attn_validate``, ...)
+take raw pointers and sizes and only marshal arguments; ``attention`` is the
+convenience call on PyTorch CUDA tensors (it allocates the outputs with torch
+and calls ``attn_fwd``).  Every step of the computation runs in the library's
+CUDA kernels; if the library is missing this module raises instead of
+computing anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+__all__ = [
+    "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED_DEVICE", "ATTN_ERR_LAUNCH",
+    "ATTN_ERR_TIMEOUT", "ATTN_ERR_CUDA",
+    "ATTN_F32", "ATTN_BF16", "ATTN_F16", "ATTN_BF16_OUT_F32", "ATTN_F16_OUT_F32",
+    "AttnError", "library_path", "load_library", "exported_symbols",
+    "attn_fwd", "attn_validate", "attn_fwd_f32_blocked", "attn_fwd_staged",
+    "attn_check_status", "attn_strerror", "attn_abi_version", "attn_test_set_hook",
+    "attention", "attention_f32_blocked", "dtype_code",
+]
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED_DEVICE = 2
+ATTN_ERR_LAUNCH = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_CUDA = 5
+
+ATTN_F32 = 0
+ATTN_BF16 = 1
+ATTN_F16 = 2
+ATTN_BF16_OUT_F32 = 3
+ATTN_F16_OUT_F32 = 4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+
+# (name, restype, argtypes) of every symbol declared in include/attn.h
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SIGS = [
+    ("attn_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    ("attn_validate", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I]),
+    ("attn_fwd_f32_blocked", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    ("attn_fwd_staged", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                             _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    ("attn_check_status", _I, [_P]),
+    ("attn_strerror", ctypes.c_char_p, [_I]),
+    ("attn_abi_version", _I, []),
+    ("attn_test_set_hook", _I, [_I, ctypes.c_uint64]),
+]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, _strerror_safe(status), status))
+
+
+def library_path() -> str:
+    return os.environ.get("ATTN_GB300_LIB", os.path.join(_HERE, "libattn.so"))
+
+
+def load_library():
+    """Load libattn.so (built by ``build.build()``); raises if it is absent."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError("libattn.so not found at %s: build it with "
+                              "online_softmax_forward_gb300.build.build()" % path)
+        lib = ctypes.CDLL(path)
+        for name, res, args in _SIGS:
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def exported_symbols():
+    return [s[0] for s in _SIGS]
+
+
+def _strerror_safe(status: int) -> str:
+    try:
+        return load_library().attn_strerror(int(status)).decode()
+    except Exception:  # pragma: no cover
+        return "status %d" % status
+
+
+def _check(status: int, where: str):
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+    return status
+
+
+# ------------------------------------------------------------------ raw ABI
+def attn_fwd(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, dtype, stream):
+    return load_library().attn_fwd(q, k, v, o, lse, B, H, Sq, Skv, d, int(causal),
+                                   float(scale), dtype, stream)
+
+
+def attn_validate(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, dtype):
+    return load_library().attn_validate(q, k, v, o, lse, B, H, Sq, Skv, d, int(causal),
+                                        float(scale), dtype)
+
+
+def attn_fwd_f32_blocked(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, block_q,
+                         block_kv, stream):
+    return load_library().attn_fwd_f32_blocked(q, k, v, o, lse, B, H, Sq, Skv, d, int(causal),
+                                               float(scale), block_q, block_kv, stream)
+
+
+def attn_fwd_staged(q_host, k_host, v_host, o_host, lse_host, dq, dk, dv, do_, dlse,
+                    B, H, Sq, Skv, d, causal, scale, dtype, stream):
+    return load_library().attn_fwd_staged(q_host, k_host, v_host, o_host, lse_host, dq, dk,
+                                           dv, do_, dlse, B, H, Sq, Skv, d, int(causal),
+                                           float(scale), dtype, stream)
+
+
+def attn_check_status(stream):
+    return load_library().attn_check_status(stream)
+
+
+def attn_strerror(status):
+    return load_library().attn_strerror(int(status)).decode()
+
+
+def attn_abi_version():
+    return load_library().attn_abi_version()
+
+
+def attn_test_set_hook(hook, timeout_ns=0):
+    return load_library().attn_test_set_hook(int(hook), int(timeout_ns))
+
+
+# ------------------------------------------------------------------ torch helpers
+def dtype_code(in_dtype, out_dtype=None) -> int:
+    """attn_dtype for torch input/output dtypes."""
+    import torch
+    if in_dtype == torch.float32:
+        if out_dtype not in (None, torch.float32):
+            raise ValueError("fp32 inputs give fp32 output")
+        return ATTN_F32
+    if in_dtype == torch.bfloat16:
+        if out_dtype in (None, torch.bfloat16):
+            return ATTN_BF16
+        if out_dtype == torch.float32:
+            return ATTN_BF16_OUT_F32
+    if in_dtype == torch.float16:
+        if out_dtype in (None, torch.float16):
+            return ATTN_F16
+        if out_dtype == torch.float32:
+            return ATTN_F16_OUT_F32
+    raise ValueError("unsupported dtypes %s -> %s" % (in_dtype, out_dtype))
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _shapes(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, S, d]")
+    B, H, Sq, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("shape mismatch q %s k %s v %s" % (tuple(q.shape), tuple(k.shape),
+                                                            tuple(v.shape)))
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+    return B, H, Sq, k.shape[2], d
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, out_dtype=None,
+              return_lse: bool = True, out=None, lse=None, stream=None):
+    """O (and LSE) for contiguous CUDA tensors q [B,H,Sq,d], k/v [B,H,Skv,d].
+
+    ``out_dtype`` = torch.float32 with bf16/fp16 inputs selects the fp32-output
+    variant.  Outputs are allocated with torch unless ``out`` / ``lse`` are
+    given."""
+    import torch
+    B, H, Sq, Skv, d = _shapes(q, k, v)
+    code = dtype_code(q.dtype, out_dtype)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share a dtype")
+    odt = {ATTN_F32: torch.float32, ATTN_BF16: torch.bfloat16, ATTN_F16: torch.float16,
+           ATTN_BF16_OUT_F32: torch.float32, ATTN_F16_OUT_F32: torch.float32}[code]
+    if out is None:
+        out = torch.empty((B, H, Sq, d), dtype=odt, device=q.device)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    sc = 0.0 if scale is None else float(scale)
+    st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                  lse.data_ptr() if lse is not None else None, B, H, Sq, Skv, d, causal,
+                  sc, code, _stream_handle(stream))
+    _check(st, "attn_fwd")
+    return (out, lse) if return_lse else out
+
+
+def attention_f32_blocked(q, k, v, block_q: int, block_kv: int, causal: bool = False,
+                          scale: float | None = None, stream=None):
+    """fp32 path with explicit tile sizes (block-size invariance tests)."""
+    import torch
+    B, H, Sq, Skv, d = _shapes(q, k, v)
+    out = torch.empty((B, H, Sq, d), dtype=torch.float32, device=q.device)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    sc = 0.0 if scale is None else float(scale)
+    st = attn_fwd_f32_blocked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr(), B, H, Sq, Skv, d, causal, sc, block_q, block_kv,
+                              _stream_handle(stream))
+    _check(st, "attn_fwd_f32_blocked")
+    return out, lse
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

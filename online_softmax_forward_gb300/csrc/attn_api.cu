@@ -1,0 +1,255 @@
+// attn_api.cu -- the extern "C" entry points of libattn.so: argument
+// validation, device check, dispatch to the fp32 or tensor-core kernel,
+// host-staged variant and the device status word.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <mutex>
+#include <stdint.h>
+#include <string.h>
+
+#include "attn.h"
+#include "attn_internal.h"
+
+namespace attn {
+
+// One status word per device (a module-scope __device__ variable: no
+// allocation).  Kernels receive its address as a parameter and atomically OR
+// error bits into it; attn_check_status reads and clears it.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_status_ptr[kMaxDevices];  // device address of g_status_word per device
+int g_hook = 0;
+uint64_t g_watchdog_ns = 1000000000ull;
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+// [lo, hi) byte ranges overlap?
+bool overlap(const void *a, size_t an, const void *b, size_t bn) {
+    if (!a || !b || an == 0 || bn == 0) return false;
+    uintptr_t a0 = (uintptr_t)a, a1 = a0 + an, b0 = (uintptr_t)b, b1 = b0 + bn;
+    return a0 < b1 && b0 < a1;
+}
+
+bool dtype_known(int dtype) { return dtype >= ATTN_F32 && dtype <= ATTN_F16_OUT_F32; }
+
+bool d_supported(int dtype, int d) {
+    if (dtype == ATTN_F32) return d == 16 || d == 32 || d == 64 || d == 128;
+    return d == 64 || d == 128;
+}
+
+int resolve_scale(float scale, int d, float *out) {
+    if (isnan(scale) || isinf(scale)) return ATTN_ERR_INVALID_ARG;
+    *out = scale > 0.f ? scale : (float)(1.0 / sqrt((double)d));
+    return ATTN_OK;
+}
+
+int cuda_to_status(cudaError_t e) {
+    if (e == cudaSuccess) return ATTN_OK;
+    if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+        return ATTN_ERR_UNSUPPORTED_DEVICE;
+    return ATTN_ERR_CUDA;
+}
+
+// The current device must be compute capability 10.3 (GB300).
+int check_device() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return ATTN_ERR_UNSUPPORTED_DEVICE;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return ATTN_ERR_UNSUPPORTED_DEVICE;
+    if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED_DEVICE;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+size_t elem_bytes_in(int dtype) { return dtype == ATTN_F32 ? 4 : 2; }
+size_t elem_bytes_out(int dtype) {
+    return (dtype == ATTN_F32 || dtype == ATTN_BF16_OUT_F32 || dtype == ATTN_F16_OUT_F32) ? 4 : 2;
+}
+
+int *status_word_device_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = (int *)p;
+    }
+    return g_status_ptr[dev];
+}
+
+int test_hook() { return g_hook; }
+uint64_t watchdog_ns() { return g_watchdog_ns; }
+
+// Validation shared by attn_validate / attn_fwd / attn_fwd_staged.
+static int validate(const void *q, const void *k, const void *v, const void *o,
+                    const float *lse, int B, int H, int Sq, int Skv, int d,
+                    int causal, float scale, int dtype, Problem *out) {
+    if (!dtype_known(dtype)) return ATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || Sq < 0 || Skv < 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!d_supported(dtype, d)) return ATTN_ERR_INVALID_ARG;
+    float sc = 0.f;
+    if (resolve_scale(scale, d, &sc) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
+    const int64_t bh = (int64_t)B * H;
+    if (bh > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+    const size_t ein = elem_bytes_in(dtype), eout = elem_bytes_out(dtype);
+    const size_t nq = (size_t)bh * Sq * d, nkv = (size_t)bh * Skv * d;
+    if (nq > 0) {
+        if (!q || !o) return ATTN_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(o, 16)) return ATTN_ERR_INVALID_ARG;
+        if (lse && !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
+    }
+    if (nkv > 0 && nq > 0) {
+        if (!k || !v) return ATTN_ERR_INVALID_ARG;
+        if (!aligned(k, 16) || !aligned(v, 16)) return ATTN_ERR_INVALID_ARG;
+    }
+    if (nq > 0) {
+        const size_t ob = nq * eout, lb = lse ? (size_t)bh * Sq * 4 : 0;
+        const void *ins[3] = {q, k, v};
+        const size_t inb[3] = {nq * ein, nkv * ein, nkv * ein};
+        for (int i = 0; i < 3; ++i) {
+            if (overlap(o, ob, ins[i], inb[i])) return ATTN_ERR_INVALID_ARG;
+            if (overlap(lse, lb, ins[i], inb[i])) return ATTN_ERR_INVALID_ARG;
+        }
+        if (overlap(o, ob, lse, lb)) return ATTN_ERR_INVALID_ARG;
+    }
+    if (out) {
+        out->B = B; out->H = H; out->Sq = Sq; out->Skv = Skv; out->d = d;
+        out->causal = causal; out->scale = sc; out->dtype = dtype;
+    }
+    return ATTN_OK;
+}
+
+static int fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
+                    const Problem &p, cudaStream_t stream) {
+    if (p.bh() == 0 || p.Sq == 0) return ATTN_OK;
+    int st = check_device();
+    if (st != ATTN_OK) return st;
+    if (p.Skv == 0) return launch_empty_keys(o, lse, p, stream);
+    if (p.dtype == ATTN_F32)
+        return launch_f32((const float *)q, (const float *)k, (const float *)v, (float *)o,
+                          lse, p, 32, 64, stream);
+    return launch_tc(q, k, v, o, lse, p, stream);
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+const char *attn_strerror(int status) {
+    switch (status) {
+    case ATTN_OK: return "success";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument (null, misaligned or overlapping pointer, bad size, head width or dtype)";
+    case ATTN_ERR_UNSUPPORTED_DEVICE: return "unsupported device: a compute capability 10.3 (GB300) GPU is required";
+    case ATTN_ERR_LAUNCH: return "kernel launch or copy failed";
+    case ATTN_ERR_TIMEOUT: return "a kernel gave up a bounded wait; its output is incomplete";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+    }
+}
+
+int attn_validate(const void *q, const void *k, const void *v, const void *o,
+                  const float *lse, int B, int H, int Sq, int Skv, int d,
+                  int causal, float scale, int dtype) {
+    return validate(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, dtype, nullptr);
+}
+
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int H, int Sq, int Skv, int d, int causal, float scale,
+             int dtype, void *stream) {
+    Problem p;
+    int st = validate(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, dtype, &p);
+    if (st != ATTN_OK) return st;
+    return fwd_impl(q, k, v, o, lse, p, (cudaStream_t)stream);
+}
+
+int attn_fwd_f32_blocked(const float *q, const float *k, const float *v,
+                         float *o, float *lse, int B, int H, int Sq, int Skv,
+                         int d, int causal, float scale, int block_q,
+                         int block_kv, void *stream) {
+    Problem p;
+    int st = validate(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, ATTN_F32, &p);
+    if (st != ATTN_OK) return st;
+    if (block_q < 1 || block_q > 128 || block_kv < 1 || block_kv > 256 ||
+        !f32_tiles_fit(d, block_q, block_kv))
+        return ATTN_ERR_INVALID_ARG;
+    if (p.bh() == 0 || p.Sq == 0) return ATTN_OK;
+    st = check_device();
+    if (st != ATTN_OK) return st;
+    if (p.Skv == 0) return launch_empty_keys(o, lse, p, (cudaStream_t)stream);
+    return launch_f32(q, k, v, o, lse, p, block_q, block_kv, (cudaStream_t)stream);
+}
+
+int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
+                    void *o_host, float *lse_host, void *dq, void *dk, void *dv,
+                    void *do_, float *dlse, int B, int H, int Sq, int Skv,
+                    int d, int causal, float scale, int dtype, void *stream) {
+    Problem p;
+    int st = validate(dq, dk, dv, do_, dlse, B, H, Sq, Skv, d, causal, scale, dtype, &p);
+    if (st != ATTN_OK) return st;
+    const size_t nq = (size_t)p.bh() * Sq * d, nkv = (size_t)p.bh() * Skv * d;
+    if (nq == 0) return ATTN_OK;
+    if (!q_host || !o_host || (nkv > 0 && (!k_host || !v_host))) return ATTN_ERR_INVALID_ARG;
+    st = check_device();
+    if (st != ATTN_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t ein = elem_bytes_in(dtype), eout = elem_bytes_out(dtype);
+    if (cudaMemcpyAsync(dq, q_host, nq * ein, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return ATTN_ERR_LAUNCH;
+    if (nkv > 0) {
+        if (cudaMemcpyAsync(dk, k_host, nkv * ein, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return ATTN_ERR_LAUNCH;
+        if (cudaMemcpyAsync(dv, v_host, nkv * ein, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return ATTN_ERR_LAUNCH;
+    }
+    st = fwd_impl(dq, dk, dv, do_, dlse, p, s);
+    if (st != ATTN_OK) return st;
+    if (cudaMemcpyAsync(o_host, do_, nq * eout, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return ATTN_ERR_LAUNCH;
+    if (lse_host && dlse) {
+        if (cudaMemcpyAsync(lse_host, dlse, (size_t)p.bh() * Sq * 4, cudaMemcpyDeviceToHost,
+                            s) != cudaSuccess)
+            return ATTN_ERR_LAUNCH;
+    }
+    return ATTN_OK;
+}
+
+int attn_check_status(void *stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_to_status(e);
+    int *dptr = status_word_device_ptr();
+    if (!dptr) return ATTN_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, dptr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(dptr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
+    if (word & kStatusTimeout) return ATTN_ERR_TIMEOUT;
+    return ATTN_OK;
+}
+
+int attn_test_set_hook(int hook, uint64_t timeout_ns) {
+    if (hook < 0 || hook > 1) return ATTN_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_hook = hook;
+    if (timeout_ns) g_watchdog_ns = timeout_ns;
+    return ATTN_OK;
+}
+
+}  // extern "C"

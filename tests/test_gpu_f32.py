@@ -1,0 +1,131 @@
+"""fp32 CUDA-core path against the fp64 oracle (max abs error <= 1e-5, the
+bound deepnotes "flash-attention-implemented-verified-and-measured" checks
+its tiled PyTorch version against in "Correctness first")."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import qkv_inputs
+from conftest import load_golden
+from gpu_util import assert_f32_parity, cast_like, run
+
+
+def f32(*xs):
+    return [cast_like(x, torch.float32) for x in xs]
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("blocks", [None, (16, 16), (7, 7)])
+def test_single_head_n64_d32(causal, blocks):
+    """Single head, B=H=1, Sq=Skv=64, d=32, uniform(-0.8, 0.8) seed 42;
+    tiles 16x16 and 7x7 (irregular)."""
+    q, k, v = f32(*qkv_inputs.uniform_qkv(1, 1, 64, 64, 32, 42))
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    o, lse = run(q, k, v, causal, blocks=blocks)
+    assert_f32_parity(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("blocks", [(8, 8), (16, 16), (13, 19), (32, 8), (1, 1), (64, 64),
+                                    (128, 256)])
+def test_p1_tile_sweep(blocks):
+    """aiml.sh "verify-tiled-attention" tile sweep: seed 7, N=64, d=16,
+    causal; the output may not depend on the tiles."""
+    q, k, v = f32(*(np.asarray(x) for x in qkv_inputs.make_qkv(64, 16, 7)))
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=True)
+    o, lse = run(q, k, v, True, blocks=blocks)
+    assert_f32_parity(o[0, 0], lse[0, 0], o_ref, lse_ref)
+
+
+def test_p1_printed_samples_on_gpu():
+    g = load_golden("p1_equivalence_check.json")
+    q, k, v = (np.asarray(x) for x in qkv_inputs.make_qkv(64, 16, 42))
+    o, _ = run(q, k, v, True, blocks=(16, 16))
+    assert np.max(np.abs(o[0, 0, 0, :4] - g["sample_row0_first4"])) <= 1e-6
+    assert np.max(np.abs(o[0, 0, -1, :4] - g["sample_last_row_first4"])) <= 1e-6
+    # causal row 0 sees only key 0: exactly v[0]
+    assert np.array_equal(o[0, 0, 0], v[0].astype(np.float32).astype(np.float64))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("skv", [64, 256, 1024])
+@pytest.mark.parametrize("boost", [1.0, 50.0])
+def test_decode_like(seed, skv, boost):
+    """Eight query rows, width 32, 64/256/1024 keys, three seeds, no mask
+    (huhohoo "tiled-online-softmax" recorded comparison) and the
+    large-score variant (q x 50)."""
+    q, k, v = qkv_inputs.uniform_qkv(1, 1, 8, skv, 32, seed)
+    q, k, v = f32(q * boost, k, v)
+    o_ref, lse_ref = oracle.attention(q, k, v)
+    for blocks in (None, (8, 32)):
+        o, lse = run(q, k, v, False, blocks=blocks)
+        assert_f32_parity(o, lse, o_ref, lse_ref)
+        assert np.all(np.isfinite(o))
+
+
+@pytest.mark.parametrize("blocks", [None, (64, 64), (32, 32)])
+def test_b2_h4_s512_d64(blocks):
+    """B=2, H=4, Sq=Skv=512, d=64, standard normal seed 0, non-causal, key
+    block 64 (deepnotes "Correctness first" shape)."""
+    q, k, v = qkv_inputs.normal_qkv(2, 4, 512, 512, 64, 0)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=False)
+    o, lse = run(q, k, v, False, blocks=blocks)
+    assert_f32_parity(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("sq,skv", [(37, 53), (53, 37), (1, 300), (300, 1), (129, 257)])
+@pytest.mark.parametrize("d", [16, 64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_shapes(sq, skv, d, causal):
+    q, k, v = qkv_inputs.uniform_qkv(2, 3, sq, skv, d, sq * 7 + skv + d)
+    q, k, v = f32(q, k, v)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    for blocks in (None, (7, 13)):
+        o, lse = run(q, k, v, causal, blocks=blocks)
+        assert_f32_parity(o, lse, o_ref, lse_ref)
+
+
+def test_overflow_logits():
+    """aiml.sh "verify-tiled-attention" overflow case: 500-valued queries,
+    scale 1/sqrt(2); padded to d=16 with zeros."""
+    q = np.zeros((2, 16)); q[:, :2] = 500.0
+    k = np.zeros((2, 16)); k[0, :2] = 1.0; k[1, :2] = 2.0
+    v = np.zeros((2, 16)); v[0, 0] = 1.0; v[1, 1] = 1.0
+    scale = 1.0 / math.sqrt(2.0)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale=scale)
+    for blocks in (None, (1, 1)):
+        o, lse = run(q, k, v, False, scale=scale, blocks=blocks)
+        assert np.all(np.isfinite(o))
+        assert_f32_parity(o[0, 0], lse[0, 0], o_ref, lse_ref)
+
+
+def test_empty_inputs():
+    import online_softmax_forward_gb300 as pkg
+    from gpu_util import ensure_built
+    ensure_built()
+    q = torch.randn(1, 2, 5, 32, device="cuda")
+    k = torch.empty(1, 2, 0, 32, device="cuda")
+    o, lse = pkg.attention(q, k, k.clone())
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(lse == -math.inf)
+    z = torch.empty(0, 2, 5, 32, device="cuda")
+    o0, _ = pkg.attention(z, z.clone(), z.clone())
+    assert o0.shape == (0, 2, 5, 32)
+    e = torch.empty(1, 1, 0, 32, device="cuda")
+    o1, _ = pkg.attention(e, torch.randn(1, 1, 4, 32, device="cuda"),
+                          torch.randn(1, 1, 4, 32, device="cuda"))
+    assert o1.shape == (1, 1, 0, 32)
+
+
+def test_deterministic_and_lse_optional():
+    import online_softmax_forward_gb300 as pkg
+    q, k, v = (t.cuda() for t in qkv_inputs.normal_qkv(2, 4, 300, 300, 64, 3))
+    o1, l1 = pkg.attention(q, k, v, causal=True)
+    o2, l2 = pkg.attention(q, k, v, causal=True)
+    o3 = pkg.attention(q, k, v, causal=True, return_lse=False)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)

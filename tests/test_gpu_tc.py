@@ -1,0 +1,185 @@
+"""bf16/fp16 tensor-core path against the fp64 oracle run on the same
+16-bit-rounded inputs.  Tolerances (fp32 output): max abs <= 1e-2, mean abs
+<= 1e-3, lse within 1e-4 * max(1, |lse|); 16-bit output: within 1e-2 plus one
+unit in the last place of the rounded oracle value."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import online_softmax_forward_gb300 as pkg
+import oracle
+import qkv_inputs
+from gpu_util import (assert_bf16_parity, assert_lse_close, assert_rounded_output, cast_like,
+                      ensure_built, run)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    # B, H, Sq, Skv, d, causal
+    (1, 1, 128, 128, 128, True),
+    (1, 2, 256, 256, 128, True),
+    (1, 2, 384, 384, 128, False),
+    (2, 2, 1000, 1000, 128, True),   # ragged: 1000 = 7*128 + 104
+    (1, 3, 300, 517, 128, True),     # Sq < Skv, bottom-right causal
+    (1, 3, 517, 300, 128, True),     # Sq > Skv: leading rows see no key
+    (1, 2, 517, 300, 128, False),
+    (1, 1, 1, 1, 128, False),
+    (1, 1, 5, 700, 128, False),      # decode-like
+    (1, 2, 640, 640, 64, True),      # d = 64
+    (2, 1, 333, 129, 64, False),
+]
+
+
+def _id(c):
+    return "B%dH%d_%dx%d_d%d_%s" % (c[0], c[1], c[2], c[3], c[4], "causal" if c[5] else "full")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("case", SMALL, ids=_id)
+def test_small_shapes_fp32_out(case, dtype):
+    B, H, Sq, Skv, d, causal = case
+    q, k, v = qkv_inputs.normal_qkv(B, H, Sq, Skv, d, seed=Sq + Skv + d, dtype=dtype)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    o, lse = run(q, k, v, causal, dtype=dtype, out_dtype=torch.float32)
+    assert_bf16_parity(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("case", SMALL[:6], ids=_id)
+def test_small_shapes_16bit_out(case, dtype):
+    B, H, Sq, Skv, d, causal = case
+    q, k, v = qkv_inputs.normal_qkv(B, H, Sq, Skv, d, seed=Sq * 3 + Skv, dtype=dtype)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    o, lse = run(q, k, v, causal, dtype=dtype)
+    assert_rounded_output(o, o_ref, dtype)
+    assert_lse_close(lse, lse_ref, 1e-4)
+
+
+def test_large_scores_stay_finite():
+    """The large-score exercise (scores x 50, q multiplied by 50).  Rows are
+    then dominated by one or two keys, and each 16-bit probability carries a
+    relative rounding error of at most 2^-9 (bf16) -- including the dominant
+    one, whose value is 2^x for a stale running maximum.  The error bound
+    that follows from that arithmetic, |o - o_ref| <= 2 * 2^-9 * max|v|, is
+    asserted here; the mean and the lse keep the standard bounds."""
+    q, k, v = qkv_inputs.normal_qkv(1, 2, 256, 512, 128, seed=9)
+    q = (q * 50).to(torch.bfloat16)
+    k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=False)
+    o, lse = run(q, k, v, False, dtype=torch.bfloat16, out_dtype=torch.float32)
+    assert np.all(np.isfinite(o))
+    err = np.abs(o - o_ref)
+    bound = 2.0 * 2.0 ** -9 * float(v.float().abs().max())
+    assert err.max() <= bound, (err.max(), bound)
+    assert err.mean() <= 1e-3
+    assert_lse_close(lse, lse_ref, 1e-4)
+
+
+def test_rising_maximum_forces_rescale():
+    """Scores that grow along the keys (q = 1, key sums ramping to 60) make
+    each row's running maximum rise by more than the lazy-rescale threshold
+    on every key tile, so the accumulator rescale runs on each of them."""
+    B, H, S, d = 1, 2, 1024, 128
+    scale = 1.0 / math.sqrt(d)
+    g = torch.Generator().manual_seed(21)
+    q = torch.ones(B, H, S, d)
+    ramp = torch.linspace(0.0, 60.0, S) / (scale * d)
+    k = ramp[None, None, :, None].expand(B, H, S, d) + 0.05 * torch.randn(B, H, S, d, generator=g)
+    v = torch.randn(B, H, S, d, generator=g)
+    q, k, v = q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+    for causal in (False, True):
+        o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+        o, lse = run(q, k, v, causal, dtype=torch.bfloat16, out_dtype=torch.float32)
+        assert_bf16_parity(o, lse, o_ref, lse_ref)
+
+
+def _sampled_parity(B, H, S, d, seed, n_random, heads=None, rows_per_head=None):
+    ensure_built()
+    q, k, v = qkv_inputs.normal_qkv(B, H, S, S, d, seed=seed, dtype=torch.bfloat16)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o32, lse = pkg.attention(qd, kd, vd, causal=True, out_dtype=torch.float32)
+    o16, lse16 = pkg.attention(qd, kd, vd, causal=True)
+    torch.cuda.synchronize()
+    assert pkg.attn_check_status(None) == pkg.ATTN_OK
+    # properties of every row
+    assert torch.isfinite(o32).all() and torch.isfinite(lse).all()
+    # row 0 sees key 0 only: its output is v[0] (exactly, once rounded to bf16)
+    assert torch.allclose(o32[:, :, 0], vd[:, :, 0].float(), rtol=1e-6, atol=0)
+    assert torch.equal(o16[:, :, 0], vd[:, :, 0])
+    assert torch.equal(lse, lse16)
+    vmin = vd.float().amin(dim=2, keepdim=True)
+    vmax = vd.float().amax(dim=2, keepdim=True)
+    assert bool(((o32 >= vmin - 1e-3) & (o32 <= vmax + 1e-3)).all())  # convex combination
+    # sampled rows against the oracle
+    BH = B * H
+    heads = range(BH) if heads is None else heads
+    qh, kh, vh = (t.reshape(BH, S, d) for t in (q, k, v))
+    rows, o_parts, l_parts = [], [], []
+    for bh in heads:
+        rs = qkv_inputs.sample_rows(S, n_random, seed=1000 + bh)
+        o_b, l_b = oracle.attention_rows(qh[bh:bh + 1], kh[bh:bh + 1], vh[bh:bh + 1],
+                                         [(0, i) for i in rs], causal=True)
+        rows += [(bh, i) for i in rs]
+        o_parts.append(o_b)
+        l_parts.append(l_b)
+    o_ref, lse_ref = np.concatenate(o_parts), np.concatenate(l_parts)
+    o32h = o32.reshape(BH, S, d).double().cpu().numpy()
+    o16h = o16.reshape(BH, S, d).double().cpu().numpy()
+    lseh = lse.reshape(BH, S).double().cpu().numpy()
+    idx = np.asarray(rows)
+    got = o32h[idx[:, 0], idx[:, 1]]
+    got_l = lseh[idx[:, 0], idx[:, 1]]
+    mx, mean = assert_bf16_parity(got, got_l, o_ref, lse_ref)
+    assert_rounded_output(o16h[idx[:, 0], idx[:, 1]], o_ref, torch.bfloat16)
+    return mx, mean, len(rows)
+
+
+def test_b1_h32_s8192_d128_causal_sampled():
+    """B=1, H=32, Sq=Skv=8192, d=128, bf16, causal, scale 1/sqrt(128):
+    every row checked for the properties above; ~200 stratified rows per
+    head (all tile boundaries) against the oracle."""
+    mx, mean, n = _sampled_parity(1, 32, 8192, 128, seed=0, n_random=64)
+    print("c4 sampled rows %d: max %.3e mean %.3e" % (n, mx, mean))
+
+
+def test_b1_h64_s32768_d128_causal_sampled():
+    """B=1, H=64, Sq=Skv=32768, d=128, bf16, causal: every row checked for
+    the properties; ~520 stratified rows in each of four heads against the
+    oracle."""
+    mx, mean, n = _sampled_parity(1, 64, 32768, 128, seed=0, n_random=8,
+                                  heads=(0, 21, 42, 63))
+    print("c5 sampled rows %d: max %.3e mean %.3e" % (n, mx, mean))
+
+
+def test_deterministic():
+    q, k, v = (t.cuda() for t in qkv_inputs.normal_qkv(1, 4, 1000, 1000, 128, 5,
+                                                        dtype=torch.bfloat16))
+    ensure_built()
+    o1, l1 = pkg.attention(q, k, v, causal=True)
+    o2, l2 = pkg.attention(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_staged_host_buffers_match_device_call():
+    """attn_fwd_staged (host buffers, copies inside the call) equals attn_fwd."""
+    ensure_built()
+    B, H, S, d = 1, 2, 640, 128
+    q, k, v = qkv_inputs.normal_qkv(B, H, S, S, d, seed=4, dtype=torch.bfloat16)
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty((B, H, S, d), dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
+    dq, dk, dv = (torch.empty_like(t, device="cuda") for t in (q, k, v))
+    do_ = torch.empty((B, H, S, d), dtype=torch.bfloat16, device="cuda")
+    dl = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    st = pkg.attn_fwd_staged(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), oh.data_ptr(),
+                             lh.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                             do_.data_ptr(), dl.data_ptr(), B, H, S, S, d, 1, 0.0,
+                             pkg.ATTN_BF16, torch.cuda.current_stream().cuda_stream)
+    assert st == pkg.ATTN_OK
+    torch.cuda.synchronize()
+    o_dev, l_dev = pkg.attention(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, o_dev.cpu()) and torch.equal(lh, l_dev.cpu())
