@@ -8,22 +8,28 @@
 //     a = a * r + P V;  l = l * r + sum P;  out = a / l
 // Tiles are 128 query rows x 128 keys.  How the work maps onto GB300:
 //
-//  * Persistent grid, one CTA per SM.  A work unit is two consecutive 128-row
-//    query tiles (Q0, Q1) of one (batch, head) slice; they share every K/V
-//    tile.  Units are handed out longest-first (causal) in a snake order.
+//  * Persistent grid, one CTA per SM, 12 warps.  A work unit is two
+//    consecutive 128-row query tiles (Q0, Q1) of one (batch, head) slice; they
+//    share every K/V tile.  Units are handed out longest-first (causal) in a
+//    snake order.
 //  * Warp 8 (producer) streams Q0/Q1 and then K_j, V_j tiles with TMA (128-byte
-//    swizzle) into a ring of shared-memory stages guarded by mbarriers.
-//  * Warp 9 (MMA issuer, one thread) runs tcgen05.mma kind::f16:
+//    swizzle) into a ring of shared-memory stages guarded by mbarriers.  Each
+//    query tile has its own Q buffer and barriers, so the next unit's Q_t is
+//    fetched as soon as the last S_t of the current unit has been computed.
+//  * Warps 9 and 10 issue the tcgen05.mma (kind::f16, fp32 accumulate) of
+//    query tile 0 and 1 respectively, as whole warps with one elected lane:
 //        S_t = Q_t K_j^T  (both operands in shared memory, fp32 in TMEM)
 //        O_t += P_t V_j   (P_t read from TMEM, V_j from shared memory)
-//    in the order S0(j) S1(j) | PV0(j) S0(j+1) | PV1(j) S1(j+1) | ..., so the
-//    tensor core works on one query tile while the other one's softmax runs.
-//    P_t is written over S_t; S_t(j+1) is issued after PV_t(j) by the same
-//    thread and relies on tcgen05.mma operations of a CTA executing in issue
-//    order.
+//    in the order S_t(j), PV_t(j), S_t(j+1), ...  Two issuers keep the tensor
+//    core fed while the softmax warps, which share their SM sub-partitions,
+//    use most issue slots (one issuing thread alone cannot).  P_t is written
+//    over S_t; S_t(j+1) is issued after PV_t(j) by the same thread and relies
+//    on the tcgen05.mma operations of one thread executing in issue order.
+//    A K/V stage is released when both issuers are done with it.
 //  * Warps 0-3 / 4-7 (softmax warpgroups, one per query tile; one thread per
-//    query row) read S from TMEM, apply the causal / tail mask, take the row
-//    max, exponentiate with ex2 (scores pre-multiplied by scale*log2 e), sum,
+//    query row, 224 registers each via setmaxnreg) read S from TMEM in two
+//    halves, apply the causal / tail mask, take the row max, exponentiate with
+//    ex2 (scores pre-multiplied by scale*log2 e, paired fp32 arithmetic), sum,
 //    write P back to TMEM as 16-bit pairs, and rescale O in TMEM when needed.
 //    The running max is updated lazily: O and l are rescaled only when the
 //    max grows by more than 2^8 (the P values then stay <= 256); O, l and m
@@ -53,10 +59,17 @@ constexpr int BM = 128;  // query rows per query tile (MMA M)
 constexpr int BN = 128;  // keys per key/value tile
 constexpr int kStages = 4;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kMmaWarp0 = 9;  // issuer of query tile 0; kMmaWarp0 + 1 issues tile 1
+constexpr int kThreads = 12 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units)
+// Register split: the block is launched with kLaunchRegs per thread; the two
+// softmax warpgroups grow to kSoftmaxRegs and the third warpgroup (producer,
+// issuers) shrinks to kOtherRegs.  The totals must match exactly.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 224;
+constexpr int kOtherRegs = 56;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs == kThreads * kLaunchRegs, "register split");
 
 template <int D>
 struct Cfg {
@@ -74,13 +87,14 @@ struct Cfg {
 };
 
 struct Bars {
-    uint64_t q_full, q_empty;
+    uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
-    uint64_t mma_done;
+    uint64_t mma_done[2];
     uint32_t tmem_base;
     int abort_flag;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct TcParams {
     void *o;
@@ -122,7 +136,8 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcParams &p) {
 }
 
 // Snake-ordered static schedule: round r hands unit r*G + c (even r) or
-// r*G + G-1-c (odd r) to CTA c.  Returns -1 when done.
+// r*G + G-1-c (odd r) to CTA c.  Returns -2 when the rounds are exhausted and
+// -1 for an empty slot of the last round.
 __device__ __forceinline__ int unit_of(int round, const TcParams &p) {
     const int G = gridDim.x, c = blockIdx.x;
     const long base = (long)round * G;
@@ -136,7 +151,9 @@ __device__ __forceinline__ int unit_of(int round, const TcParams &p) {
 //   1024 B apart (SBO); the K offset inside the atom is added to the start
 //   address.  MN-major operands (V for P.V): 64 contiguous N elements per
 //   128-byte row, 8 K-rows per 1024-B atom (SBO), atoms along N 16 KB apart
-//   (LBO).
+//   (LBO).  The start address occupies the low 14 bits (address / 16), so
+//   an offset inside the same shared-memory window is added to the
+//   descriptor directly.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
@@ -204,10 +221,65 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // Keeps the compiler from reading tcgen05.ld destination registers before
-// tcgen05.wait::ld.
-__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+// tcgen05.wait::ld (and from recycling tcgen05.st source registers before
+// tcgen05.wait::st when placed after it).
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// A 64-key half tile of S held as two 32-column tcgen05.ld results.
+struct Half {
+    uint32_t a[32], b[32];
+};
+
+__device__ __forceinline__ void tmem_ld_half(uint32_t taddr, Half &h) {
+    ptx::tmem_ld32(taddr, h.a);
+    ptx::tmem_ld32(taddr + 32, h.b);
+}
+__device__ __forceinline__ void fence_half(Half &h) {
+    reg_fence(h.a);
+    reg_fence(h.b);
+}
+
+// Masks keys >= limit of a 64-key half tile starting at key kv0 and returns
+// its maximum (raw scores).
+__device__ __forceinline__ float half_max(Half &h, int kv0, int limit) {
+    if (kv0 + 64 > limit) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if (kv0 + i >= limit) h.a[i] = __float_as_uint(-INFINITY);
+            if (kv0 + 32 + i >= limit) h.b[i] = __float_as_uint(-INFINITY);
+        }
+    }
+    float x0 = __uint_as_float(h.a[0]), x1 = __uint_as_float(h.a[1]);
+    float x2 = __uint_as_float(h.b[0]), x3 = __uint_as_float(h.b[1]);
+#pragma unroll
+    for (int i = 2; i + 3 < 30; i += 4) {  // elements 2..29 of a and b
+        x0 = ptx::max3(x0, __uint_as_float(h.a[i]), __uint_as_float(h.a[i + 1]));
+        x1 = ptx::max3(x1, __uint_as_float(h.a[i + 2]), __uint_as_float(h.a[i + 3]));
+        x2 = ptx::max3(x2, __uint_as_float(h.b[i]), __uint_as_float(h.b[i + 1]));
+        x3 = ptx::max3(x3, __uint_as_float(h.b[i + 2]), __uint_as_float(h.b[i + 3]));
+    }
+    // elements 30 and 31 of a and b
+    return fmaxf(ptx::max3(x0, __uint_as_float(h.a[30]), __uint_as_float(h.a[31])),
+                 ptx::max3(fmaxf(x1, x3), x2, fmaxf(__uint_as_float(h.b[30]), __uint_as_float(h.b[31]))));
+}
+
+// P = 2^(s * sl2 - mb) for 32 keys: packed 16-bit pairs into pk, fp32
+// partial sums into acc.
+template <bool kBF16>
+__device__ __forceinline__ void exp32(const uint32_t (&r)[32], float sl2, float mb,
+                                      uint32_t *pk, float2 (&acc)[4]) {
+    const float2 sc = make_float2(sl2, sl2), nb = make_float2(-mb, -mb);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc, nb);
+        const float p0 = ptx::ex2_approx(x.x), p1 = ptx::ex2_approx(x.y);
+        acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
+        pk[i] = pack2<kBF16>(p0, p1);
+    }
 }
 
 template <int D, bool kBF16>
@@ -229,19 +301,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     // ---------------------------------------------------------------- setup
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar(bars->q_full), 1);
-        ptx::mbar_init(bar(bars->q_empty), 1);
-        for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(bar(bars->kv_full[s]), 1);
-            ptx::mbar_init(bar(bars->kv_empty[s]), 1);
-        }
         for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(bar(bars->q_full[t]), 1);
+            ptx::mbar_init(bar(bars->q_empty[t]), 1);
             ptx::mbar_init(bar(bars->s_full[t]), 1);
             ptx::mbar_init(bar(bars->p_full[t]), 128);
             ptx::mbar_init(bar(bars->o_full[t]), 1);
             ptx::mbar_init(bar(bars->o_empty[t]), 128);
+            ptx::mbar_init(bar(bars->mma_done[t]), 1);
         }
-        ptx::mbar_init(bar(bars->mma_done), 1);
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(bar(bars->kv_full[s]), 1);
+            ptx::mbar_init(bar(bars->kv_empty[s]), 2);  // one arrival per issuer
+        }
         bars->abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -250,7 +322,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), kTmemCols);
         ptx::tmem_relinquish();
     }
@@ -259,12 +331,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
+    // Each role changes its register budget at the top of its own branch, so
+    // the compiler sees which limit holds for which code.
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
+        ptx::setmaxnreg_dec<kOtherRegs>();
         if (lane == 0) {
-            uint32_t pos = 0, qn = 0;
-            bool loaded_q = false;
-            uint32_t last_q_par = 0;
+            uint32_t pos = 0;
+            uint32_t qn[2] = {0, 0}, q_last_par[2] = {0, 0};
+            bool q_loaded[2] = {false, false};
             bool ok = true;
             for (int round = 0; ok; ++round) {
                 const int u = unit_of(round, p);
@@ -273,15 +348,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const Unit w = decode_unit(u, p);
                 const int nmax = max(w.nkv[0], w.nkv[1]);
                 if (nmax == 0) continue;
-                if (!watch.wait(bar(bars->q_empty), (qn & 1) ^ 1)) { ok = false; break; }
-                ptx::mbar_arrive_expect_tx(bar(bars->q_full), 2 * C::kTileBytes);
-                for (int t = 0; t < 2; ++t)
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (w.nkv[t] == 0) continue;
+                    if (!watch.wait(bar(bars->q_empty[t]), (qn[t] & 1) ^ 1)) { ok = false; break; }
+                    ptx::mbar_arrive_expect_tx(bar(bars->q_full[t]), C::kTileBytes);
                     for (int c = 0; c < C::kChunks; ++c)
                         ptx::tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
-                                         bar(bars->q_full), c * 64, w.q0 + t * BM, w.bh);
-                last_q_par = qn & 1;
-                loaded_q = true;
-                ++qn;
+                                         bar(bars->q_full[t]), c * 64, w.q0 + t * BM, w.bh);
+                    q_last_par[t] = qn[t] & 1;
+                    q_loaded[t] = true;
+                    ++qn[t];
+                }
                 for (int j = 0; j < nmax && ok; ++j) {
                     for (int which = 0; which < 2; ++which) {  // K_j then V_j
                         const int s = pos % kStages;
@@ -303,105 +380,89 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const uint32_t last = s + ((pos - 1 - s) / kStages) * kStages;  // last use of s
                 watch.drain(bar(bars->kv_full[s]), (last / kStages) & 1);
             }
-            if (loaded_q) watch.drain(bar(bars->q_full), last_q_par);
+            for (int t = 0; t < 2; ++t)
+                if (q_loaded[t]) watch.drain(bar(bars->q_full[t]), q_last_par[t]);
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t kIdescS = idesc_f16(kBF16, BM, BN, false);
-            constexpr uint32_t kIdescO = idesc_f16(kBF16, BM, D, true);
-            uint32_t pos = 0, qn = 0;
-            uint32_t pn[2] = {0, 0}, on[2] = {0, 0};
-            bool ok = true;
-            bool first_unit = true;
-
-            auto issue_s = [&](int t, int stage) {
-                const uint32_t d_tmem = tmem + C::col_s(t);
-                const uint32_t a0 = sQ + t * C::kTileBytes, b0 = sKV + stage * C::kTileBytes;
+    } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
+        // ------------------------------------------------------------ MMA issuer of tile t
+        // The whole warp runs this loop; one elected lane issues each MMA and commit.
+        ptx::setmaxnreg_dec<kOtherRegs>();
+        // a wait's outcome is made warp-uniform so that the warp stays converged
+        auto wait_all = [&](uint32_t b, uint32_t parity) {
+            return __all_sync(0xffffffffu, watch.wait(b, parity));
+        };
+        const int t = warp - kMmaWarp0;
+        constexpr uint32_t kIdescS = idesc_f16(kBF16, BM, BN, false);
+        constexpr uint32_t kIdescO = idesc_f16(kBF16, BM, D, true);
+        const uint64_t dq = sdesc(sQ + t * C::kTileBytes, 16, 1024);
+        const uint64_t dk = sdesc(sKV, 16, 1024);
+        const uint64_t dv = sdesc(sKV, C::kChunkBytes, 1024);
+        const uint32_t tS = tmem + C::col_s(t), tO = tmem + C::col_o(t);
+        uint32_t pos = 0, qn = 0, pn = 0, on = 0;
+        bool ok = true;
+        bool first = true;
+        for (int round = 0; ok; ++round) {
+            const int u = unit_of(round, p);
+            if (u == -2) break;
+            if (u < 0) continue;
+            const Unit w = decode_unit(u, p);
+            const int nmax = max(w.nkv[0], w.nkv[1]);
+            const int my = w.nkv[t];
+            if (nmax == 0) continue;
+            if (my > 0) {
+                if (!wait_all(bar(bars->q_full[t]), qn & 1)) { ok = false; break; }
+                ++qn;
+            }
+            for (int j = 0; j < nmax; ++j, pos += 2) {
+                const int stK = pos % kStages, stV = (pos + 1) % kStages;
+                const uint32_t parK = (pos / kStages) & 1, parV = ((pos + 1) / kStages) & 1;
+                if (!wait_all(bar(bars->kv_full[stK]), parK)) { ok = false; break; }
+                if (j >= my) {
+                    // this tile needs no more keys: release the stages in order
+                    ptx::mbar_arrive_warp(bar(bars->kv_empty[stK]));
+                    if (!wait_all(bar(bars->kv_full[stV]), parV)) { ok = false; break; }
+                    ptx::mbar_arrive_warp(bar(bars->kv_empty[stV]));
+                    continue;
+                }
+                ptx::tc_fence_after();
+                // S_t(j) = Q_t K_j^T
+                const uint64_t dkj = dk + (uint64_t)((stK * C::kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                    ptx::mma_ss(d_tmem, sdesc(a0 + koff, 16, 1024), sdesc(b0 + koff, 16, 1024),
-                                kIdescS, kk > 0 ? 1u : 0u);
+                    const uint32_t koff = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+                    ptx::mma_ss_warp(tS, dq + koff, dkj + koff, kIdescS, kk > 0 ? 1u : 0u);
                 }
-            };
-            auto issue_pv = [&](int t, int stage, bool acc) {
-                const uint32_t d_tmem = tmem + C::col_o(t);
-                const uint32_t b0 = sKV + stage * C::kTileBytes;
+                const bool skip = p.hook == 1 && first && t == 0 && blockIdx.x == 0;
+                if (!skip) ptx::mma_commit_warp(bar(bars->s_full[t]));
+                first = false;
+                ptx::mma_commit_warp(bar(bars->kv_empty[stK]));
+                if (j == my - 1) ptx::mma_commit_warp(bar(bars->q_empty[t]));
+                // O_t += P_t(j) V_j once the softmax has written P_t(j)
+                if (!wait_all(bar(bars->kv_full[stV]), parV)) { ok = false; break; }
+                if (!wait_all(bar(bars->p_full[t]), pn & 1)) { ok = false; break; }
+                ++pn;
+                if (j == 0) {
+                    if (!wait_all(bar(bars->o_empty[t]), (on & 1) ^ 1)) { ok = false; break; }
+                    ++on;
+                }
+                ptx::tc_fence_after();
+                const uint64_t dvj = dv + (uint64_t)((stV * C::kTileBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint32_t a_tmem = tmem + C::col_s(t) + kk * 8;  // 16 keys = 8 columns
-                    ptx::mma_ts(d_tmem, a_tmem, sdesc(b0 + kk * 16 * 128, C::kChunkBytes, 1024),
-                                kIdescO, (acc || kk > 0) ? 1u : 0u);
-                }
-            };
-
-            for (int round = 0; ok; ++round) {
-                const int u = unit_of(round, p);
-                if (u == -2) break;
-                if (u < 0) continue;
-                const Unit w = decode_unit(u, p);
-                const int nmax = max(w.nkv[0], w.nkv[1]);
-                if (nmax == 0) continue;
-                if (!watch.wait(bar(bars->q_full), qn & 1)) { ok = false; break; }
-                ++qn;
-                ptx::tc_fence_after();
-                // K_0: S0(0), S1(0)
-                uint32_t posK = pos++;
-                int stK = posK % kStages;
-                if (!watch.wait(bar(bars->kv_full[stK]), (posK / kStages) & 1)) { ok = false; break; }
-                ptx::tc_fence_after();
-                for (int t = 0; t < 2; ++t) {
-                    if (w.nkv[t] > 0) {
-                        issue_s(t, stK);
-                        const bool skip = p.hook == 1 && first_unit && t == 0 && blockIdx.x == 0;
-                        if (!skip) ptx::mma_commit(bar(bars->s_full[t]));
-                    }
-                }
-                ptx::mma_commit(bar(bars->kv_empty[stK]));
-                first_unit = false;
-                for (int j = 0; j < nmax && ok; ++j) {
-                    const uint32_t posV = pos++;
-                    const int stV = posV % kStages;
-                    if (!watch.wait(bar(bars->kv_full[stV]), (posV / kStages) & 1)) { ok = false; break; }
-                    const bool has_next = j + 1 < nmax;
-                    if (has_next) {
-                        posK = pos++;
-                        stK = posK % kStages;
-                        if (!watch.wait(bar(bars->kv_full[stK]), (posK / kStages) & 1)) { ok = false; break; }
-                    }
-                    ptx::tc_fence_after();
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        if (j >= w.nkv[t]) continue;
-                        if (!watch.wait(bar(bars->p_full[t]), pn[t] & 1)) { ok = false; break; }
-                        ++pn[t];
-                        if (j == 0) {
-                            if (!watch.wait(bar(bars->o_empty[t]), (on[t] & 1) ^ 1)) { ok = false; break; }
-                            ++on[t];
-                        }
-                        ptx::tc_fence_after();
-                        issue_pv(t, stV, j > 0);
-                        if (j == w.nkv[t] - 1) ptx::mma_commit(bar(bars->o_full[t]));
-                        if (j + 1 < w.nkv[t]) {
-                            issue_s(t, stK);
-                            ptx::mma_commit(bar(bars->s_full[t]));
-                        }
-                    }
-                    if (!ok) break;
-                    ptx::mma_commit(bar(bars->kv_empty[stV]));
-                    if (has_next) ptx::mma_commit(bar(bars->kv_empty[stK]));
-                }
-                if (!ok) break;
-                ptx::mma_commit(bar(bars->q_empty));
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    ptx::mma_ts_warp(tO, tS + kk * 8, dvj + (uint64_t)((kk * 16 * 128) >> 4), kIdescO,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
+                ptx::mma_commit_warp(bar(bars->kv_empty[stV]));
+                if (j == my - 1) ptx::mma_commit_warp(bar(bars->o_full[t]));
             }
-            // teardown: every MMA issued by this thread has completed
-            ptx::mma_commit(bar(bars->mma_done));
-            watch.drain(bar(bars->mma_done), 0);
         }
+        // teardown: every MMA issued by this warp has completed
+        ptx::mma_commit_warp(bar(bars->mma_done[t]));
+        watch.drain(bar(bars->mma_done[t]), 0);
         __syncwarp();
-    } else {
+    } else if (warp < kProducerWarp) {
         // ------------------------------------------------------------ softmax
+        ptx::setmaxnreg_inc<kSoftmaxRegs>();
         const int t = warp >> 2;        // query tile of this warpgroup
         const int wq = warp & 3;        // TMEM lane quarter of this warp
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
@@ -428,34 +489,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ++sn;
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 ptx::tc_fence_after();
-                uint32_t r[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, r[c]);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) reg_fence(r[c]);
-
-                float s[128];
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
                 const int kv0 = j * BN;
-                if (kv0 + BN > limit) {
-#pragma unroll
-                    for (int i = 0; i < 128; ++i)
-                        if (kv0 + i >= limit) s[i] = -INFINITY;
-                }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-                for (int i = 4; i < 128; i += 4) {
-                    mx0 = fmaxf(mx0, s[i]);
-                    mx1 = fmaxf(mx1, s[i + 1]);
-                    mx2 = fmaxf(mx2, s[i + 2]);
-                    mx3 = fmaxf(mx3, s[i + 3]);
-                }
-                const float tile_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-                const float m_new = fmaxf(m, tile_max);
+                Half ra, rb;
+                tmem_ld_half(tS, ra);
+                ptx::tmem_wait_ld();
+                fence_half(ra);
+                tmem_ld_half(tS + 64, rb);  // in flight while the first half is reduced
+                const float mxa = half_max(ra, kv0, limit);
+                ptx::tmem_wait_ld();
+                fence_half(rb);
+                const float mxb = half_max(rb, kv0 + 64, limit);
+                const float m_new = fmaxf(m, fmaxf(mxa, mxb) * sl2);
                 bool rescale = false;
                 float alpha = 1.f;
                 if (m == -INFINITY) {
@@ -468,6 +512,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O_t holds P V of tiles < j (complete: S_t(j) was issued after them)
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
@@ -475,30 +520,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         ptx::tmem_wait_ld();
                         reg_fence(o);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+                            o[i] = __float_as_uint(v.x);
+                            o[i + 1] = __float_as_uint(v.y);
+                        }
                         ptx::tmem_st32(tO + c * 32, o);
+                        ptx::tmem_wait_st();
                     }
-                    ptx::tmem_wait_st();
                 }
                 const float mb = (m == -INFINITY) ? 0.f : m;
-                float sum0 = 0.f, sum1 = 0.f;
-                uint32_t pk[2][32];
-#pragma unroll
-                for (int i = 0; i < 128; i += 2) {
-                    const float p0 = ptx::ex2_approx(fmaf(s[i], sl2, -mb));
-                    const float p1 = ptx::ex2_approx(fmaf(s[i + 1], sl2, -mb));
-                    sum0 += p0;
-                    sum1 += p1;
-                    pk[i >> 6][(i >> 1) & 31] = pack2<kBF16>(p0, p1);
-                }
-                l += sum0 + sum1;
-                __syncwarp();  // tcgen05.st needs the whole warp converged
-                ptx::tmem_st32(tS, pk[0]);
-                ptx::tmem_st32(tS + 32, pk[1]);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                uint32_t pa[32], pb[32];
+                exp32<kBF16>(ra.a, sl2, mb, pa, acc);
+                exp32<kBF16>(ra.b, sl2, mb, pa + 16, acc);
+                ptx::tmem_st32(tS, pa);  // P keys 0..63 -> columns 0..31
+                exp32<kBF16>(rb.a, sl2, mb, pb, acc);
+                exp32<kBF16>(rb.b, sl2, mb, pb + 16, acc);
+                ptx::tmem_st32(tS + 32, pb);
                 ptx::tmem_wait_st();
+                reg_fence(pa);
+                reg_fence(pb);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(bars->p_full[t]));
+                const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
+                l += (s01.x + s01.y) + (s23.x + s23.y);
             }
             if (!ok) break;
 
@@ -556,13 +603,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ptx::mbar_arrive(bar(bars->o_empty[t]));
             }
         }
+    } else {
+        // warp 11: no role; it only gives up its registers
+        ptx::setmaxnreg_dec<kOtherRegs>();
     }
 
     // ---------------------------------------------------------------- teardown
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+    if (warp == kMmaWarp0) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side
@@ -634,6 +684,16 @@ int launch_typed(const void *q, const void *k, const void *v, void *o, float *ls
     if (sms <= 0) return ATTN_ERR_CUDA;
     const int grid = (int)(n_units < sms ? n_units : sms);
     auto kern = attn_tc_kernel<D, kBF16>;
+    // The register split inside the kernel (setmaxnreg) needs exactly the pool
+    // it was sized for; a build with another entry register count would block
+    // in setmaxnreg.inc, so it is refused here instead of launched.
+    static int regs_ok = -1;
+    if (regs_ok < 0) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return ATTN_ERR_UNSUPPORTED_DEVICE;
+        regs_ok = (fa.numRegs == kLaunchRegs && fa.maxThreadsPerBlock >= kThreads) ? 1 : 0;
+    }
+    if (!regs_ok) return ATTN_ERR_LAUNCH;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return ATTN_ERR_LAUNCH;
