@@ -243,9 +243,9 @@ __device__ __forceinline__ void fence_half(Half &h) {
     reg_fence(h.b);
 }
 
-// Masks keys >= limit of a 64-key half tile starting at key kv0 and returns
-// its maximum (raw scores).
-__device__ __forceinline__ float half_max(Half &h, int kv0, int limit) {
+// Keys >= limit of a 64-key half tile starting at key kv0 get a score of
+// -inf (excluded), so that they contribute exp(-inf) = 0.
+__device__ __forceinline__ void mask_half(Half &h, int kv0, int limit) {
     if (kv0 + 64 > limit) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -253,6 +253,10 @@ __device__ __forceinline__ float half_max(Half &h, int kv0, int limit) {
             if (kv0 + 32 + i >= limit) h.b[i] = __float_as_uint(-INFINITY);
         }
     }
+}
+
+// Maximum raw score of a 64-key half tile.
+__device__ __forceinline__ float max_half(const Half &h) {
     float x0 = __uint_as_float(h.a[0]), x1 = __uint_as_float(h.a[1]);
     float x2 = __uint_as_float(h.b[0]), x3 = __uint_as_float(h.b[1]);
 #pragma unroll
@@ -294,7 +298,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t sQ = ptx::smem_addr(smem + C::kOffQ);
     const uint32_t sKV = ptx::smem_addr(smem + C::kOffKV);
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The warp index is broadcast from lane 0 so that the compiler knows it is
+    // warp-uniform: role branches and every value derived from it (MMA
+    // descriptors, tensor-memory addresses) can then live in uniform registers.
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+    const int lane = threadIdx.x & 31;
     const Watch watch{&bars->abort_flag, p.status, p.timeout_ns};
 
     auto bar = [&](uint64_t &b) { return ptx::smem_addr(&b); };
@@ -329,7 +337,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    const uint32_t tmem = bars->tmem_base;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, bars->tmem_base, 0);
 
     // Each role changes its register budget at the top of its own branch, so
     // the compiler sees which limit holds for which code.
@@ -402,6 +410,58 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         uint32_t pos = 0, qn = 0, pn = 0, on = 0;
         bool ok = true;
         bool first = true;
+        auto stage_of = [&](uint32_t at, int &st) {
+            st = at % kStages;
+            return (at / kStages) & 1;
+        };
+        // S_t(jj) = Q_t K_jj^T from ring position `at` (key tile jj of the unit)
+        auto slot_s = [&](uint32_t at, int jj, int my) {
+            int st;
+            const uint32_t par = stage_of(at, st);
+            if (!wait_all(bar(bars->kv_full[st]), par)) return false;
+            if (jj >= my) {  // this tile needs no more keys: release the stage in order
+                ptx::mbar_arrive_warp(bar(bars->kv_empty[st]));
+                return true;
+            }
+            ptx::tc_fence_after();
+            const uint64_t dkj = dk + (uint64_t)((st * C::kTileBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t koff = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+                ptx::mma_ss_warp(tS, dq + koff, dkj + koff, kIdescS, kk > 0 ? 1u : 0u);
+            }
+            const bool skip = p.hook == 1 && first && t == 0 && blockIdx.x == 0;
+            if (!skip) ptx::mma_commit_warp(bar(bars->s_full[t]));
+            first = false;
+            ptx::mma_commit_warp(bar(bars->kv_empty[st]));
+            if (jj == my - 1) ptx::mma_commit_warp(bar(bars->q_empty[t]));
+            return true;
+        };
+        // O_t += P_t(jj) V_jj once the softmax has written P_t(jj)
+        auto slot_pv = [&](uint32_t at, int jj, int my) {
+            int st;
+            const uint32_t par = stage_of(at, st);
+            if (!wait_all(bar(bars->kv_full[st]), par)) return false;
+            if (jj >= my) {
+                ptx::mbar_arrive_warp(bar(bars->kv_empty[st]));
+                return true;
+            }
+            if (!wait_all(bar(bars->p_full[t]), pn & 1)) return false;
+            ++pn;
+            if (jj == 0) {
+                if (!wait_all(bar(bars->o_empty[t]), (on & 1) ^ 1)) return false;
+                ++on;
+            }
+            ptx::tc_fence_after();
+            const uint64_t dvj = dv + (uint64_t)((st * C::kTileBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+                ptx::mma_ts_warp(tO, tS + kk * 8, dvj + (uint64_t)((kk * 16 * 128) >> 4), kIdescO,
+                                 (jj > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_commit_warp(bar(bars->kv_empty[st]));
+            if (jj == my - 1) ptx::mma_commit_warp(bar(bars->o_full[t]));
+            return true;
+        };
         for (int round = 0; ok; ++round) {
             const int u = unit_of(round, p);
             if (u == -2) break;
@@ -414,47 +474,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (!wait_all(bar(bars->q_full[t]), qn & 1)) { ok = false; break; }
                 ++qn;
             }
-            for (int j = 0; j < nmax; ++j, pos += 2) {
-                const int stK = pos % kStages, stV = (pos + 1) % kStages;
-                const uint32_t parK = (pos / kStages) & 1, parV = ((pos + 1) / kStages) & 1;
-                if (!wait_all(bar(bars->kv_full[stK]), parK)) { ok = false; break; }
-                if (j >= my) {
-                    // this tile needs no more keys: release the stages in order
-                    ptx::mbar_arrive_warp(bar(bars->kv_empty[stK]));
-                    if (!wait_all(bar(bars->kv_full[stV]), parV)) { ok = false; break; }
-                    ptx::mbar_arrive_warp(bar(bars->kv_empty[stV]));
-                    continue;
-                }
-                ptx::tc_fence_after();
-                // S_t(j) = Q_t K_j^T
-                const uint64_t dkj = dk + (uint64_t)((stK * C::kTileBytes) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-                    ptx::mma_ss_warp(tS, dq + koff, dkj + koff, kIdescS, kk > 0 ? 1u : 0u);
-                }
-                const bool skip = p.hook == 1 && first && t == 0 && blockIdx.x == 0;
-                if (!skip) ptx::mma_commit_warp(bar(bars->s_full[t]));
-                first = false;
-                ptx::mma_commit_warp(bar(bars->kv_empty[stK]));
-                if (j == my - 1) ptx::mma_commit_warp(bar(bars->q_empty[t]));
-                // O_t += P_t(j) V_j once the softmax has written P_t(j)
-                if (!wait_all(bar(bars->kv_full[stV]), parV)) { ok = false; break; }
-                if (!wait_all(bar(bars->p_full[t]), pn & 1)) { ok = false; break; }
-                ++pn;
-                if (j == 0) {
-                    if (!wait_all(bar(bars->o_empty[t]), (on & 1) ^ 1)) { ok = false; break; }
-                    ++on;
-                }
-                ptx::tc_fence_after();
-                const uint64_t dvj = dv + (uint64_t)((stV * C::kTileBytes) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    ptx::mma_ts_warp(tO, tS + kk * 8, dvj + (uint64_t)((kk * 16 * 128) >> 4), kIdescO,
-                                     (j > 0 || kk > 0) ? 1u : 0u);
-                ptx::mma_commit_warp(bar(bars->kv_empty[stV]));
-                if (j == my - 1) ptx::mma_commit_warp(bar(bars->o_full[t]));
-            }
+            // K_j sits at ring position pos + 2j, V_j at pos + 2j + 1.  Every
+            // stage is waited for and released in ring order, also by a tile
+            // that needs fewer key tiles than the other.
+            ok = slot_s(pos, 0, my);
+            for (int j = 0; j < nmax && ok; ++j)
+                ok = slot_pv(pos + 2 * j + 1, j, my) &&
+                     (j + 1 >= nmax || slot_s(pos + 2 * j + 2, j + 1, my));
+            pos += 2 * nmax;
         }
         // teardown: every MMA issued by this warp has completed
         ptx::mma_commit_warp(bar(bars->mma_done[t]));
@@ -495,11 +522,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ptx::tmem_wait_ld();
                 fence_half(ra);
                 tmem_ld_half(tS + 64, rb);  // in flight while the first half is reduced
-                const float mxa = half_max(ra, kv0, limit);
+                mask_half(ra, kv0, limit);
+                const float mxa = max_half(ra);
                 ptx::tmem_wait_ld();
                 fence_half(rb);
-                const float mxb = half_max(rb, kv0 + 64, limit);
-                const float m_new = fmaxf(m, fmaxf(mxa, mxb) * sl2);
+                mask_half(rb, kv0 + 64, limit);
+                const float m_new = fmaxf(m, fmaxf(mxa, max_half(rb)) * sl2);
                 bool rescale = false;
                 float alpha = 1.f;
                 if (m == -INFINITY) {
@@ -535,9 +563,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 uint32_t pa[32], pb[32];
                 exp32<kBF16>(ra.a, sl2, mb, pa, acc);
                 exp32<kBF16>(ra.b, sl2, mb, pa + 16, acc);
-                ptx::tmem_st32(tS, pa);  // P keys 0..63 -> columns 0..31
                 exp32<kBF16>(rb.a, sl2, mb, pb, acc);
                 exp32<kBF16>(rb.b, sl2, mb, pb + 16, acc);
+                __syncwarp();  // tcgen05.st needs the whole warp converged
+                ptx::tmem_st32(tS, pa);  // P keys 0..63 -> columns 0..31
                 ptx::tmem_st32(tS + 32, pb);
                 ptx::tmem_wait_st();
                 reg_fence(pa);
