@@ -12,29 +12,29 @@
 //    consecutive 128-row query tiles (Q0, Q1) of one (batch, head) slice; they
 //    share every K/V tile.  Units are handed out longest-first (causal) in a
 //    snake order.
-//  * Warp 8 (producer) streams Q0/Q1 and then K_j, V_j tiles with TMA (128-byte
-//    swizzle) into a ring of shared-memory stages guarded by mbarriers.  Each
-//    query tile has its own Q buffer and barriers, so the next unit's Q_t is
-//    fetched as soon as the last S_t of the current unit has been computed.
+//  * Warp 8 (producer) streams Q0/Q1 and the K/V tiles with TMA (128-byte
+//    swizzle) into a ring of shared-memory stages guarded by mbarriers, in
+//    the order the tensor core consumes them: K_0, then K_{j+1}, V_j for each
+//    j.  Each query tile has its own Q buffer and barriers, so the next unit's
+//    Q_t is fetched as soon as the last S_t of the current unit is computed.
 //  * Warps 9 and 10 issue the tcgen05.mma (kind::f16, fp32 accumulate) of
 //    query tile 0 and 1 respectively, as whole warps with one elected lane:
-//        S_t = Q_t K_j^T  (both operands in shared memory, fp32 in TMEM)
-//        O_t += P_t V_j   (P_t read from TMEM, V_j from shared memory)
-//    in the order S_t(j), PV_t(j), S_t(j+1), ...  Two issuers keep the tensor
-//    core fed while the softmax warps, which share their SM sub-partitions,
-//    use most issue slots (one issuing thread alone cannot).  P_t is written
-//    over S_t; S_t(j+1) is issued after PV_t(j) by the same thread and relies
-//    on the tcgen05.mma operations of one thread executing in issue order.
+//        S_t = Q_t K_j^T  (shared-memory operands, fp32 result in TMEM)
+//        O_t += P_t V_j   (P_t and V_j in shared memory, O_t in TMEM)
+//    S_t(j+1) is issued as soon as the softmax has copied S_t(j) out of tensor
+//    memory, so the tensor core computes the next scores while the softmax
+//    exponentiates the current ones; PV_t(j) follows once P_t(j) is written.
 //    A K/V stage is released when both issuers are done with it.
 //  * Warps 0-3 / 4-7 (softmax warpgroups, one per query tile; one thread per
 //    query row, 224 registers each via setmaxnreg) read S from TMEM in two
 //    halves, apply the causal / tail mask, take the row max, exponentiate with
 //    ex2 (scores pre-multiplied by scale*log2 e, paired fp32 arithmetic), sum,
-//    write P back to TMEM as 16-bit pairs, and rescale O in TMEM when needed.
-//    The running max is updated lazily: O and l are rescaled only when the
-//    max grows by more than 2^8 (the P values then stay <= 256); O, l and m
-//    always refer to the same stale max, so the result is the same softmax.
-//    After the last tile they write O / l and lse = m + ln l.
+//    and write P as 16-bit values into a shared-memory tile in the MMA's
+//    128-byte-swizzled layout.  The running max is updated lazily: O and l are
+//    rescaled (O in TMEM, after the previous P.V has completed) only when the
+//    max grows by more than 2^8, so P stays <= 256; O, l and m always refer
+//    to the same stale max, so the result is the same softmax.  After the
+//    last tile they write O / l and lse = m + ln l.
 //  * Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0, O1 after.
 //  * Every mbarrier wait is bounded (globaltimer).  On expiry the CTA sets an
 //    abort flag, records ATTN timeout in the status word, lets every role
@@ -57,7 +57,6 @@ namespace {
 
 constexpr int BM = 128;  // query rows per query tile (MMA M)
 constexpr int BN = 128;  // keys per key/value tile
-constexpr int kStages = 4;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp0 = 9;  // issuer of query tile 0; kMmaWarp0 + 1 issues tile 1
 constexpr int kThreads = 12 * 32;
@@ -75,21 +74,29 @@ template <int D>
 struct Cfg {
     static_assert(D == 64 || D == 128, "head width");
     static constexpr int kChunks = D / 64;            // 128-byte swizzle atoms along d
-    static constexpr int kChunkBytes = BN * 128;      // one atom column of a tile: 16 KB
+    static constexpr int kChunkBytes = BN * 128;      // one atom column of a 128-row tile: 16 KB
     static constexpr int kTileBytes = kChunks * kChunkBytes;  // Q, K or V tile
+    static constexpr int kPBytes = 2 * kChunkBytes;   // P tile: 128 rows x 128 keys, 16-bit
+    static constexpr int kStages = D == 128 ? 3 : 6;  // K/V ring depth (fills 227 KB)
     static constexpr int kOffQ = 0;                   // Q0, Q1
-    static constexpr int kOffKV = 2 * kTileBytes;     // ring stages
+    static constexpr int kOffP = 2 * kTileBytes;      // P0, P1
+    static constexpr int kOffKV = kOffP + 2 * kPBytes;  // ring stages
     static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
     static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
     // tensor-memory columns of S_t and O_t
     __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
     __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? (uint32_t)D : 0u); }
 };
+constexpr int kMaxStages = 6;
 
 struct Bars {
     uint64_t q_full[2], q_empty[2];
-    uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+    uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
+    uint64_t s_full[2];   // S_t computed (MMA commit)
+    uint64_t s_free[2];   // S_t copied to registers by the softmax (128 arrivals)
+    uint64_t p_full[2];   // P_t written to shared memory (128 arrivals)
+    uint64_t p_free[2];   // P_t . V done: P buffer free, O_t up to date (MMA commit)
+    uint64_t o_empty[2];  // epilogue has read O_t (128 arrivals)
     uint64_t mma_done[2];
     uint32_t tmem_base;
     int abort_flag;
@@ -291,11 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
     using C = Cfg<D>;
+    constexpr int kStages = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars *bars = reinterpret_cast<Bars *>(smem + C::kOffBar);
     const uint32_t sQ = ptx::smem_addr(smem + C::kOffQ);
+    const uint32_t sP = ptx::smem_addr(smem + C::kOffP);
     const uint32_t sKV = ptx::smem_addr(smem + C::kOffKV);
 
     // The warp index is broadcast from lane 0 so that the compiler knows it is
@@ -313,8 +322,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ptx::mbar_init(bar(bars->q_full[t]), 1);
             ptx::mbar_init(bar(bars->q_empty[t]), 1);
             ptx::mbar_init(bar(bars->s_full[t]), 1);
+            ptx::mbar_init(bar(bars->s_free[t]), 128);
             ptx::mbar_init(bar(bars->p_full[t]), 128);
-            ptx::mbar_init(bar(bars->o_full[t]), 1);
+            ptx::mbar_init(bar(bars->p_free[t]), 1);
             ptx::mbar_init(bar(bars->o_empty[t]), 128);
             ptx::mbar_init(bar(bars->mma_done[t]), 1);
         }
@@ -339,6 +349,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     ptx::tc_fence_after();
     const uint32_t tmem = __shfl_sync(0xffffffffu, bars->tmem_base, 0);
 
+    // Ring position of the K/V tiles of a unit with n key tiles whose first
+    // tile sits at position `base`: the order is K_0, then K_{j+1}, V_j for
+    // j = 0 .. n-2, then V_{n-1} -- the order in which the MMAs consume them.
+    auto pos_k = [](uint32_t base, int j) { return base + (j == 0 ? 0u : (uint32_t)(2 * j - 1)); };
+    auto pos_v = [](uint32_t base, int j, int n) {
+        return base + (j + 1 < n ? (uint32_t)(2 * j + 2) : (uint32_t)(2 * j + 1));
+    };
+
     // Each role changes its register budget at the top of its own branch, so
     // the compiler sees which limit holds for which code.
     if (warp == kProducerWarp) {
@@ -349,6 +367,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             uint32_t qn[2] = {0, 0}, q_last_par[2] = {0, 0};
             bool q_loaded[2] = {false, false};
             bool ok = true;
+            auto load_kv = [&](const CUtensorMap *tm, int j, int bh) {
+                const int s = pos % kStages;
+                if (!watch.wait(bar(bars->kv_empty[s]), ((pos / kStages) & 1) ^ 1)) return false;
+                ptx::mbar_arrive_expect_tx(bar(bars->kv_full[s]), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    ptx::tma_load_3d(sKV + s * C::kTileBytes + c * C::kChunkBytes, tm,
+                                     bar(bars->kv_full[s]), c * 64, j * BN, bh);
+                ++pos;
+                return true;
+            };
             for (int round = 0; ok; ++round) {
                 const int u = unit_of(round, p);
                 if (u == -2) break;
@@ -367,21 +395,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     q_loaded[t] = true;
                     ++qn[t];
                 }
-                for (int j = 0; j < nmax && ok; ++j) {
-                    for (int which = 0; which < 2; ++which) {  // K_j then V_j
-                        const int s = pos % kStages;
-                        if (!watch.wait(bar(bars->kv_empty[s]), ((pos / kStages) & 1) ^ 1)) {
-                            ok = false;
-                            break;
-                        }
-                        ptx::mbar_arrive_expect_tx(bar(bars->kv_full[s]), C::kTileBytes);
-                        const CUtensorMap *tm = which ? &tm_v : &tm_k;
-                        for (int c = 0; c < C::kChunks; ++c)
-                            ptx::tma_load_3d(sKV + s * C::kTileBytes + c * C::kChunkBytes, tm,
-                                             bar(bars->kv_full[s]), c * 64, j * BN, w.bh);
-                        ++pos;
-                    }
-                }
+                ok = ok && load_kv(&tm_k, 0, w.bh);
+                for (int j = 0; j < nmax && ok; ++j)
+                    ok = (j + 1 >= nmax || load_kv(&tm_k, j + 1, w.bh)) && load_kv(&tm_v, j, w.bh);
             }
             // teardown: wait until every load this thread issued has landed
             for (uint32_t s = 0; s < (uint32_t)kStages && s < pos; ++s) {
@@ -404,18 +420,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         constexpr uint32_t kIdescS = idesc_f16(kBF16, BM, BN, false);
         constexpr uint32_t kIdescO = idesc_f16(kBF16, BM, D, true);
         const uint64_t dq = sdesc(sQ + t * C::kTileBytes, 16, 1024);
+        const uint64_t dp = sdesc(sP + t * C::kPBytes, 16, 1024);
         const uint64_t dk = sdesc(sKV, 16, 1024);
         const uint64_t dv = sdesc(sKV, C::kChunkBytes, 1024);
         const uint32_t tS = tmem + C::col_s(t), tO = tmem + C::col_o(t);
-        uint32_t pos = 0, qn = 0, pn = 0, on = 0;
+        uint32_t pos = 0, qn = 0, sn = 0, pn = 0, on = 0;
         bool ok = true;
         bool first = true;
         auto stage_of = [&](uint32_t at, int &st) {
             st = at % kStages;
             return (at / kStages) & 1;
         };
-        // S_t(jj) = Q_t K_jj^T from ring position `at` (key tile jj of the unit)
-        auto slot_s = [&](uint32_t at, int jj, int my) {
+        // S_t(jj) = Q_t K_jj^T, K_jj at ring position `at`
+        auto issue_s = [&](uint32_t at, int jj, int my) {
             int st;
             const uint32_t par = stage_of(at, st);
             if (!wait_all(bar(bars->kv_full[st]), par)) return false;
@@ -423,6 +440,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ptx::mbar_arrive_warp(bar(bars->kv_empty[st]));
                 return true;
             }
+            // the softmax must have copied the previous S_t out of tensor memory
+            if (sn > 0 && !wait_all(bar(bars->s_free[t]), (sn - 1) & 1)) return false;
             ptx::tc_fence_after();
             const uint64_t dkj = dk + (uint64_t)((st * C::kTileBytes) >> 4);
 #pragma unroll
@@ -433,12 +452,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const bool skip = p.hook == 1 && first && t == 0 && blockIdx.x == 0;
             if (!skip) ptx::mma_commit_warp(bar(bars->s_full[t]));
             first = false;
+            ++sn;
             ptx::mma_commit_warp(bar(bars->kv_empty[st]));
             if (jj == my - 1) ptx::mma_commit_warp(bar(bars->q_empty[t]));
             return true;
         };
         // O_t += P_t(jj) V_jj once the softmax has written P_t(jj)
-        auto slot_pv = [&](uint32_t at, int jj, int my) {
+        auto issue_pv = [&](uint32_t at, int jj, int my) {
             int st;
             const uint32_t par = stage_of(at, st);
             if (!wait_all(bar(bars->kv_full[st]), par)) return false;
@@ -448,18 +468,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             if (!wait_all(bar(bars->p_full[t]), pn & 1)) return false;
             ++pn;
-            if (jj == 0) {
+            if (jj == 0) {  // the epilogue of the previous unit has read O_t
                 if (!wait_all(bar(bars->o_empty[t]), (on & 1) ^ 1)) return false;
                 ++on;
             }
             ptx::tc_fence_after();
             const uint64_t dvj = dv + (uint64_t)((st * C::kTileBytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-                ptx::mma_ts_warp(tO, tS + kk * 8, dvj + (uint64_t)((kk * 16 * 128) >> 4), kIdescO,
+            for (int kk = 0; kk < BN / 16; ++kk) {
+                const uint32_t koff = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+                ptx::mma_ss_warp(tO, dp + koff, dvj + (uint64_t)((kk * 16 * 128) >> 4), kIdescO,
                                  (jj > 0 || kk > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit_warp(bar(bars->p_free[t]));
             ptx::mma_commit_warp(bar(bars->kv_empty[st]));
-            if (jj == my - 1) ptx::mma_commit_warp(bar(bars->o_full[t]));
             return true;
         };
         for (int round = 0; ok; ++round) {
@@ -474,13 +496,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (!wait_all(bar(bars->q_full[t]), qn & 1)) { ok = false; break; }
                 ++qn;
             }
-            // K_j sits at ring position pos + 2j, V_j at pos + 2j + 1.  Every
-            // stage is waited for and released in ring order, also by a tile
-            // that needs fewer key tiles than the other.
-            ok = slot_s(pos, 0, my);
+            // every stage is waited for and released in ring order, also by a
+            // tile that needs fewer key tiles than the other
+            ok = issue_s(pos_k(pos, 0), 0, my);
             for (int j = 0; j < nmax && ok; ++j)
-                ok = slot_pv(pos + 2 * j + 1, j, my) &&
-                     (j + 1 >= nmax || slot_s(pos + 2 * j + 2, j + 1, my));
+                ok = (j + 1 >= nmax || issue_s(pos_k(pos, j + 1), j + 1, my)) &&
+                     issue_pv(pos_v(pos, j, nmax), j, my);
             pos += 2 * nmax;
         }
         // teardown: every MMA issued by this warp has completed
@@ -492,12 +513,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         ptx::setmaxnreg_inc<kSoftmaxRegs>();
         const int t = warp >> 2;        // query tile of this warpgroup
         const int wq = warp & 3;        // TMEM lane quarter of this warp
+        const int r = wq * 32 + lane;   // row of this thread inside the tile
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_base + C::col_s(t);
         const uint32_t tO = tmem + lane_base + C::col_o(t);
+        const uint32_t pRow = sP + t * C::kPBytes + r * 128;  // this row in both P atom columns
+        const uint32_t swz = (uint32_t)(r & 7);               // 128-byte swizzle phase of the row
         const float sl2 = p.scale_log2;
         const int off = p.Skv - p.Sq;
-        uint32_t sn = 0, ofn = 0;
+        uint32_t sn = 0, pfn = 0;
         bool ok = true;
 
         for (int round = 0; ok; ++round) {
@@ -506,7 +530,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (u < 0) continue;
             const Unit w = decode_unit(u, p);
             const int nk = w.nkv[t];
-            const int row = w.q0 + t * BM + wq * 32 + lane;  // query index of this thread
+            const int row = w.q0 + t * BM + r;  // query index of this thread
             const int limit = p.causal ? min(p.Skv, row + off + 1) : p.Skv;  // keys < limit visible
             float m = -INFINITY;  // running max, log2-scaled units
             float l = 0.f;        // running normaliser relative to m
@@ -526,6 +550,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const float mxa = max_half(ra);
                 ptx::tmem_wait_ld();
                 fence_half(rb);
+                // S_t is in registers: the next S_t may be written
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(bars->s_free[t]));
                 mask_half(rb, kv0 + 64, limit);
                 const float m_new = fmaxf(m, fmaxf(mxa, max_half(rb)) * sl2);
                 bool rescale = false;
@@ -538,8 +565,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     m = m_new;
                     l *= alpha;
                 }
+                // P_t(j-1) . V must be complete before O_t is rescaled or the P
+                // buffer is overwritten
+                bool pv_done = (j == 0);
                 if (__any_sync(0xffffffffu, rescale)) {
-                    // O_t holds P V of tiles < j (complete: S_t(j) was issued after them)
+                    if (!pv_done) {
+                        const bool g2 = watch.wait(bar(bars->p_free[t]), pfn & 1);
+                        ++pfn;
+                        pv_done = true;
+                        if (!__all_sync(0xffffffffu, g2)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                    }
                     const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
@@ -565,12 +601,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 exp32<kBF16>(ra.b, sl2, mb, pa + 16, acc);
                 exp32<kBF16>(rb.a, sl2, mb, pb, acc);
                 exp32<kBF16>(rb.b, sl2, mb, pb + 16, acc);
-                __syncwarp();  // tcgen05.st needs the whole warp converged
-                ptx::tmem_st32(tS, pa);  // P keys 0..63 -> columns 0..31
-                ptx::tmem_st32(tS + 32, pb);
-                ptx::tmem_wait_st();
-                reg_fence(pa);
-                reg_fence(pb);
+                if (!pv_done) {
+                    const bool g2 = watch.wait(bar(bars->p_free[t]), pfn & 1);
+                    ++pfn;
+                    if (!__all_sync(0xffffffffu, g2)) { ok = false; break; }
+                }
+                // P row into the K-major, 128-byte-swizzled tile: 16-byte chunk c
+                // of a 128-byte row is stored at chunk c ^ (row mod 8)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    ptx::st_shared_v4(pRow + ((((uint32_t)c) ^ swz) << 4), pa[4 * c], pa[4 * c + 1],
+                                      pa[4 * c + 2], pa[4 * c + 3]);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    ptx::st_shared_v4(pRow + C::kChunkBytes + ((((uint32_t)c) ^ swz) << 4), pb[4 * c],
+                                      pb[4 * c + 1], pb[4 * c + 2], pb[4 * c + 3]);
+                ptx::fence_proxy_async_smem();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(bars->p_full[t]));
                 const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
@@ -579,9 +625,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (!ok) break;
 
             // epilogue: O / l and lse for the rows of this thread
-            if (nk > 0) {
-                const bool got = watch.wait(bar(bars->o_full[t]), ofn & 1);
-                ++ofn;
+            if (nk > 0) {  // the last P_t . V of the unit has completed
+                const bool got = watch.wait(bar(bars->p_free[t]), pfn & 1);
+                ++pfn;
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 ptx::tc_fence_after();
             }
