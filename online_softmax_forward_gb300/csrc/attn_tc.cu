@@ -599,8 +599,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 uint32_t pa[32], pb[32];
                 exp32<kBF16>(ra.a, sl2, mb, pa, acc);
                 exp32<kBF16>(ra.b, sl2, mb, pa + 16, acc);
-                exp32<kBF16>(rb.a, sl2, mb, pb, acc);
-                exp32<kBF16>(rb.b, sl2, mb, pb + 16, acc);
                 if (!pv_done) {
                     const bool g2 = watch.wait(bar(bars->p_free[t]), pfn & 1);
                     ++pfn;
@@ -612,6 +610,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int c = 0; c < 8; ++c)
                     ptx::st_shared_v4(pRow + ((((uint32_t)c) ^ swz) << 4), pa[4 * c], pa[4 * c + 1],
                                       pa[4 * c + 2], pa[4 * c + 3]);
+                exp32<kBF16>(rb.a, sl2, mb, pb, acc);
+                exp32<kBF16>(rb.b, sl2, mb, pb + 16, acc);
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     ptx::st_shared_v4(pRow + C::kChunkBytes + ((((uint32_t)c) ^ swz) << 4), pb[4 * c],
