@@ -22,6 +22,9 @@ Contents
     huhohoo "tiled-online-softmax" ("A failing baseline").
 ``estimate_hbm_bytes`` (module ``oracle.access``)
     The logical K/V/Q/O access model of aiml.sh "verify-tiled-attention".
+``merge_partials`` (module ``oracle.merge``)
+    The online-softmax update applied to whole partial results over disjoint
+    key sets (huhohoo "tiled-online-softmax", "Online normalization").
 """
 from __future__ import annotations
 
@@ -33,6 +36,7 @@ import numpy as np
 
 from . import build as _build
 from .access import estimate_hbm_bytes  # noqa: F401
+from .merge import merge_partials  # noqa: F401
 from .tiled import block_normalised_average, tiled_attention  # noqa: F401
 
 _lib = None
