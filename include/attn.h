@@ -49,6 +49,7 @@
 #ifndef ATTN_GB300_ATTN_H
 #define ATTN_GB300_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -126,6 +127,81 @@ int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
                     void *o_host, float *lse_host, void *dq, void *dk, void *dv,
                     void *do_, float *dlse, int B, int H, int Sq, int Skv,
                     int d, int causal, float scale, int dtype, void *stream);
+
+/*
+ * Split-KV forward for a few query rows per head (decode)
+ * --------------------------------------------------------
+ * The keys of every (batch, head) are cut into n_splits contiguous ranges of
+ * equal length (a multiple of 32 keys); each range is processed by its own
+ * CTAs on CUDA cores (fp32 arithmetic for every input type), which write a
+ * partial result -- the softmax-weighted average of the range's values and
+ * the log-sum-exp of its scaled scores -- into `workspace`; attn_merge's
+ * kernel then combines the partial results of every row.  The result is the
+ * same operation as attn_fwd: only the order of the sums differs (the pages'
+ * point that the tiling, here the split, changes nothing but rounding:
+ * aiml.sh "verify-tiled-attention", tile-size sweep; huhohoo
+ * "tiled-online-softmax", block size seven).
+ */
+
+/*
+ * attn_splitkv_workspace_size -- bytes of the workspace attn_fwd_splitkv
+ * needs: 4 * n_splits * B * H * Sq * (d + 1) (partial outputs
+ * [n_splits][B*H][Sq][d] followed by partial lse [n_splits][B*H][Sq], fp32).
+ * Host only.  d in {16, 32, 64, 128}; 1 <= n_splits <= 256.
+ */
+int attn_splitkv_workspace_size(int B, int H, int Sq, int d, int n_splits, size_t *bytes);
+
+/*
+ * attn_splitkv_plan -- the split count the library would pick on the current
+ * device (enough CTAs to fill every SM several times over, at least two
+ * 32-key tiles per warp in each split) and, if workspace_bytes is not NULL,
+ * the workspace size for it.  Needs a compute capability 10.3 device.
+ */
+int attn_splitkv_plan(int B, int H, int Sq, int Skv, int d, int dtype, int *n_splits,
+                      size_t *workspace_bytes);
+
+/*
+ * attn_fwd_splitkv -- attn_fwd computed by key splits.
+ *
+ * Arguments and layouts as attn_fwd, except:
+ *   d          in {16, 32, 64, 128} for every dtype;
+ *   Sq         <= 524280;
+ *   n_splits   1 .. 256 (see attn_splitkv_plan); empty trailing splits are
+ *              skipped;
+ *   workspace  device memory of at least attn_splitkv_workspace_size bytes,
+ *              16-byte aligned, owned by the caller and not overlapping any
+ *              other argument; its contents are scratch (overwritten).
+ *              May be NULL when Skv == 0.
+ * Enqueues two kernels on `stream` (partial results, merge).  Returns
+ * ATTN_ERR_INVALID_ARG for a missing, small, misaligned or overlapping
+ * workspace; otherwise as attn_fwd.
+ */
+int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int H, int Sq, int Skv, int d, int causal, float scale,
+                     int dtype, int n_splits, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/*
+ * attn_merge -- combines partial attention results of the same query rows
+ * over disjoint key sets (key splits, or key shards held by different
+ * devices) into the result over the union of the keys.  Each partial result
+ * is the state (m, l, a) of the online softmax in the form o_part = a / l,
+ * lse_part = m + ln l; the merge is the update of huhohoo
+ * "tiled-online-softmax" ("Online normalization") applied to whole states:
+ *   M = max_p lse_p,  w_p = exp(lse_p - M),
+ *   o = sum_p w_p o_p / sum_p w_p,  lse = M + ln(sum_p w_p).
+ * A part with lse = -inf (no visible key) contributes nothing; a row whose
+ * parts are all -inf gets o = 0 and lse = -inf.
+ *
+ *   o_parts    [n_parts][rows][d] fp32, device memory
+ *   lse_parts  [n_parts][rows]    fp32, natural log
+ *   o          [rows][d] of out_dtype: ATTN_F32, ATTN_BF16 or ATTN_F16
+ *   lse        [rows] fp32, or NULL
+ * fp32 arithmetic; asynchronous on `stream`.  Outputs must not overlap the
+ * inputs or each other (ATTN_ERR_INVALID_ARG).
+ */
+int attn_merge(const float *o_parts, const float *lse_parts, int n_parts, int64_t rows, int d,
+               void *o, float *lse, int out_dtype, void *stream);
 
 /*
  * attn_check_status -- synchronises `stream`, then reads and clears the

@@ -21,7 +21,8 @@ __all__ = [
     "AttnError", "library_path", "load_library", "exported_symbols",
     "attn_fwd", "attn_validate", "attn_fwd_f32_blocked", "attn_fwd_staged",
     "attn_check_status", "attn_strerror", "attn_abi_version", "attn_test_set_hook",
-    "attention", "attention_f32_blocked", "dtype_code",
+    "attn_splitkv_workspace_size", "attn_splitkv_plan", "attn_fwd_splitkv", "attn_merge",
+    "attention", "attention_f32_blocked", "attention_splitkv", "merge", "dtype_code",
 ]
 
 ATTN_OK = 0
@@ -54,6 +55,12 @@ _SIGS = [
     ("attn_strerror", ctypes.c_char_p, [_I]),
     ("attn_abi_version", _I, []),
     ("attn_test_set_hook", _I, [_I, ctypes.c_uint64]),
+    ("attn_splitkv_workspace_size", _I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
+    ("attn_splitkv_plan", _I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I),
+                               ctypes.POINTER(ctypes.c_size_t)]),
+    ("attn_fwd_splitkv", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P,
+                              ctypes.c_size_t, _P]),
+    ("attn_merge", _I, [_P, _P, _I, ctypes.c_int64, _I, _P, _P, _I, _P]),
 ]
 
 
@@ -141,6 +148,34 @@ def attn_test_set_hook(hook, timeout_ns=0):
     return load_library().attn_test_set_hook(int(hook), int(timeout_ns))
 
 
+def attn_splitkv_workspace_size(B, H, Sq, d, n_splits):
+    """Returns (status, bytes)."""
+    n = ctypes.c_size_t(0)
+    st = load_library().attn_splitkv_workspace_size(B, H, Sq, d, n_splits, ctypes.byref(n))
+    return st, n.value
+
+
+def attn_splitkv_plan(B, H, Sq, Skv, d, dtype):
+    """Returns (status, n_splits, workspace_bytes)."""
+    n = ctypes.c_int(0)
+    b = ctypes.c_size_t(0)
+    st = load_library().attn_splitkv_plan(B, H, Sq, Skv, d, dtype, ctypes.byref(n),
+                                          ctypes.byref(b))
+    return st, n.value, b.value
+
+
+def attn_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, dtype, n_splits,
+                     workspace, workspace_bytes, stream):
+    return load_library().attn_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Skv, d, int(causal),
+                                           float(scale), dtype, int(n_splits), workspace,
+                                           int(workspace_bytes), stream)
+
+
+def attn_merge(o_parts, lse_parts, n_parts, rows, d, o, lse, out_dtype, stream):
+    return load_library().attn_merge(o_parts, lse_parts, int(n_parts), int(rows), int(d), o,
+                                     lse, int(out_dtype), stream)
+
+
 # ------------------------------------------------------------------ torch helpers
 def dtype_code(in_dtype, out_dtype=None) -> int:
     """attn_dtype for torch input/output dtypes."""
@@ -225,3 +260,53 @@ def attention_f32_blocked(q, k, v, block_q: int, block_kv: int, causal: bool = F
 
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
+
+
+def attention_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
+                      out_dtype=None, n_splits: int | None = None, workspace=None,
+                      stream=None):
+    """Split-KV forward (few query rows, long key sequences).  The workspace is
+    a torch uint8 CUDA tensor, allocated here unless given; ``n_splits`` is
+    the library's choice unless given.  Returns (o, lse)."""
+    import torch
+    B, H, Sq, Skv, d = _shapes(q, k, v)
+    code = dtype_code(q.dtype, out_dtype)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share a dtype")
+    if n_splits is None:
+        st, n_splits, _ = attn_splitkv_plan(B, H, Sq, Skv, d, code)
+        _check(st, "attn_splitkv_plan")
+    st, need = attn_splitkv_workspace_size(B, H, Sq, d, n_splits)
+    _check(st, "attn_splitkv_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    odt = {ATTN_F32: torch.float32, ATTN_BF16: torch.bfloat16, ATTN_F16: torch.float16,
+           ATTN_BF16_OUT_F32: torch.float32, ATTN_F16_OUT_F32: torch.float32}[code]
+    out = torch.empty((B, H, Sq, d), dtype=odt, device=q.device)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    sc = 0.0 if scale is None else float(scale)
+    st = attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr(), B, H, Sq, Skv, d, causal, sc, code, n_splits,
+                          workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(st, "attn_fwd_splitkv")
+    return out, lse
+
+
+def merge(o_parts, lse_parts, out_dtype=None, stream=None):
+    """attn_merge on torch tensors: o_parts [n, rows, d] fp32, lse_parts
+    [n, rows] fp32 -> (o [rows, d], lse [rows])."""
+    import torch
+    if o_parts.dim() != 3 or lse_parts.shape != o_parts.shape[:2]:
+        raise ValueError("o_parts [n, rows, d] and lse_parts [n, rows] expected")
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+        raise ValueError("partial results are fp32")
+    o_parts, lse_parts = o_parts.contiguous(), lse_parts.contiguous()
+    n, rows, d = o_parts.shape
+    odt = torch.float32 if out_dtype is None else out_dtype
+    code = {torch.float32: ATTN_F32, torch.bfloat16: ATTN_BF16, torch.float16: ATTN_F16}[odt]
+    out = torch.empty((rows, d), dtype=odt, device=o_parts.device)
+    lse = torch.empty((rows,), dtype=torch.float32, device=o_parts.device)
+    st = attn_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n, rows, d, out.data_ptr(),
+                    lse.data_ptr(), code, _stream_handle(stream))
+    _check(st, "attn_merge")
+    return out, lse

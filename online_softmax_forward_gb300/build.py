@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattn.so")
-SOURCES = ["attn_api.cu", "attn_f32.cu", "attn_tc.cu"]
+SOURCES = ["attn_api.cu", "attn_f32.cu", "attn_splitkv.cu", "attn_tc.cu"]
 HEADERS = ["attn_internal.h", "sm100_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

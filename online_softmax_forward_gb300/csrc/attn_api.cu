@@ -89,14 +89,16 @@ int *status_word_device_ptr() {
 int test_hook() { return g_hook; }
 uint64_t watchdog_ns() { return g_watchdog_ns; }
 
-// Validation shared by attn_validate / attn_fwd / attn_fwd_staged.
+// Validation shared by attn_validate / attn_fwd / attn_fwd_staged /
+// attn_fwd_splitkv.  any_width: every head width of the fp32 path is allowed
+// for every dtype (the split-KV path).
 static int validate(const void *q, const void *k, const void *v, const void *o,
                     const float *lse, int B, int H, int Sq, int Skv, int d,
-                    int causal, float scale, int dtype, Problem *out) {
+                    int causal, float scale, int dtype, Problem *out, bool any_width = false) {
     if (!dtype_known(dtype)) return ATTN_ERR_INVALID_ARG;
     if (B < 0 || H < 0 || Sq < 0 || Skv < 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
-    if (!d_supported(dtype, d)) return ATTN_ERR_INVALID_ARG;
+    if (!d_supported(any_width ? ATTN_F32 : dtype, d)) return ATTN_ERR_INVALID_ARG;
     float sc = 0.f;
     if (resolve_scale(scale, d, &sc) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
     const int64_t bh = (int64_t)B * H;
@@ -127,6 +129,15 @@ static int validate(const void *q, const void *k, const void *v, const void *o,
         out->causal = causal; out->scale = sc; out->dtype = dtype;
     }
     return ATTN_OK;
+}
+
+// Bytes of the split-KV workspace: partial outputs [n][B*H][Sq][d] and
+// partial lse [n][B*H][Sq], fp32.  Returns false on overflow.
+static bool splitkv_bytes(int64_t bh, int Sq, int d, int n_splits, size_t *bytes) {
+    const double est = (double)n_splits * (double)bh * (double)Sq * (double)(d + 1) * 4.0;
+    if (est > 9.0e18) return false;
+    *bytes = (size_t)n_splits * (size_t)bh * (size_t)Sq * (size_t)(d + 1) * 4u;
+    return true;
 }
 
 static int fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -225,6 +236,86 @@ int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
             return ATTN_ERR_LAUNCH;
     }
     return ATTN_OK;
+}
+
+int attn_splitkv_workspace_size(int B, int H, int Sq, int d, int n_splits, size_t *bytes) {
+    if (!bytes || B < 0 || H < 0 || Sq < 0 || !d_supported(ATTN_F32, d)) return ATTN_ERR_INVALID_ARG;
+    if (n_splits < 1 || n_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+    return splitkv_bytes((int64_t)B * H, Sq, d, n_splits, bytes) ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
+int attn_splitkv_plan(int B, int H, int Sq, int Skv, int d, int dtype, int *n_splits,
+                      size_t *workspace_bytes) {
+    Problem p;
+    int st = validate(nullptr, nullptr, nullptr, nullptr, nullptr, 0, 0, 0, 0, d, 0, 0.f, dtype,
+                      &p, true);
+    if (st != ATTN_OK || !n_splits || B < 0 || H < 0 || Sq < 0 || Skv < 0)
+        return ATTN_ERR_INVALID_ARG;
+    st = check_device();
+    if (st != ATTN_OK) return st;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    p.B = B; p.H = H; p.Sq = Sq; p.Skv = Skv;
+    *n_splits = splitkv_choose(p, sms);
+    if (workspace_bytes)
+        return attn_splitkv_workspace_size(B, H, Sq, d, *n_splits, workspace_bytes);
+    return ATTN_OK;
+}
+
+int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int H, int Sq, int Skv, int d, int causal, float scale,
+                     int dtype, int n_splits, void *workspace, size_t workspace_bytes,
+                     void *stream) {
+    Problem p;
+    int st = validate(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, dtype, &p, true);
+    if (st != ATTN_OK) return st;
+    if (n_splits < 1 || n_splits > kMaxSplits || Sq > kMaxSplitRows) return ATTN_ERR_INVALID_ARG;
+    if (p.bh() == 0 || Sq == 0) return ATTN_OK;
+    size_t need = 0;
+    if (!splitkv_bytes(p.bh(), Sq, d, n_splits, &need)) return ATTN_ERR_INVALID_ARG;
+    if (Skv > 0) {
+        if (!workspace || !aligned(workspace, 16) || workspace_bytes < need)
+            return ATTN_ERR_INVALID_ARG;
+        const size_t nq = (size_t)p.bh() * Sq * d, nkv = (size_t)p.bh() * Skv * d;
+        const size_t ein = elem_bytes_in(dtype), eout = elem_bytes_out(dtype);
+        if (overlap(workspace, need, q, nq * ein) || overlap(workspace, need, k, nkv * ein) ||
+            overlap(workspace, need, v, nkv * ein) || overlap(workspace, need, o, nq * eout) ||
+            overlap(workspace, need, lse, lse ? (size_t)p.bh() * Sq * 4 : 0))
+            return ATTN_ERR_INVALID_ARG;
+    }
+    st = check_device();
+    if (st != ATTN_OK) return st;
+    if (Skv == 0) return launch_empty_keys(o, lse, p, (cudaStream_t)stream);
+    float *part_o = (float *)workspace;
+    float *part_lse = part_o + (size_t)n_splits * p.bh() * Sq * d;
+    return launch_splitkv(q, k, v, o, lse, p, n_splits, part_o, part_lse, (cudaStream_t)stream);
+}
+
+int attn_merge(const float *o_parts, const float *lse_parts, int n_parts, int64_t rows, int d,
+               void *o, float *lse, int out_dtype, void *stream) {
+    if (n_parts < 1 || rows < 0 || d < 1) return ATTN_ERR_INVALID_ARG;
+    if (out_dtype != ATTN_F32 && out_dtype != ATTN_BF16 && out_dtype != ATTN_F16)
+        return ATTN_ERR_INVALID_ARG;
+    if (rows == 0) return ATTN_OK;
+    const size_t eout = out_dtype == ATTN_F32 ? 4 : 2;
+    const double est = (double)n_parts * (double)rows * (double)d * 4.0;
+    if (est > 9.0e18) return ATTN_ERR_INVALID_ARG;
+    const size_t po_b = (size_t)n_parts * rows * d * 4, pl_b = (size_t)n_parts * rows * 4;
+    const size_t o_b = (size_t)rows * d * eout, l_b = lse ? (size_t)rows * 4 : 0;
+    if (!o_parts || !lse_parts || !o) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(o_parts, 4) || !aligned(lse_parts, 4) || !aligned(o, eout) ||
+        (lse && !aligned(lse, 4)))
+        return ATTN_ERR_INVALID_ARG;
+    if (overlap(o, o_b, o_parts, po_b) || overlap(o, o_b, lse_parts, pl_b) ||
+        overlap(lse, l_b, o_parts, po_b) || overlap(lse, l_b, lse_parts, pl_b) ||
+        overlap(o, o_b, lse, l_b))
+        return ATTN_ERR_INVALID_ARG;
+    const int st = check_device();
+    if (st != ATTN_OK) return st;
+    return launch_merge(o_parts, lse_parts, n_parts, rows, d, o, lse, out_dtype,
+                        (cudaStream_t)stream);
 }
 
 int attn_check_status(void *stream) {

@@ -32,6 +32,22 @@ bool f32_tiles_fit(int d, int block_q, int block_kv);
 int launch_tc(const void *q, const void *k, const void *v, void *o, float *lse,
               const Problem &p, cudaStream_t stream);
 
+// Split-KV path for few query rows (attn_splitkv.cu).
+constexpr int kSplitRowBlock = 8;  // query rows per split-KV CTA when Sq > 1
+constexpr int kMaxSplits = 256;    // upper bound of n_splits
+constexpr int kMaxSplitRows = 65535 * kSplitRowBlock;  // grid limit on Sq
+int splitkv_row_block(int Sq);
+void splitkv_chunking(int Skv, int n_splits, int *chunk, int *n_eff);
+int splitkv_choose(const Problem &p, int sms);
+// part_o [n_splits][B*H][Sq][d] and part_lse [n_splits][B*H][Sq] fp32.
+int launch_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                   const Problem &p, int n_splits, float *part_o, float *part_lse,
+                   cudaStream_t stream);
+// Merges [n_parts][rows][d] / [n_parts][rows] into o [rows][d] (out_dtype
+// ATTN_F32, ATTN_BF16 or ATTN_F16) and lse [rows] (may be null).
+int launch_merge(const float *po, const float *pl, int n_parts, int64_t rows, int d, void *o,
+                 float *lse, int out_dtype, cudaStream_t stream);
+
 // Writes o = 0 and lse = -inf (Skv == 0).
 int launch_empty_keys(void *o, float *lse, const Problem &p, cudaStream_t stream);
 

@@ -103,3 +103,72 @@ def test_hook_rejects_unknown_values(lib):
 
 def test_default_scale():
     assert pkg.default_scale(128) == 1.0 / math.sqrt(128)
+
+
+# ------------------------------------------------------------------ split-KV and merge
+def test_splitkv_workspace_size(lib):
+    st, n = pkg.attn_splitkv_workspace_size(2, 4, 8, 32, 3)
+    assert st == pkg.ATTN_OK and n == 4 * 3 * 2 * 4 * 8 * 33
+    st, n = pkg.attn_splitkv_workspace_size(0, 4, 8, 32, 3)
+    assert st == pkg.ATTN_OK and n == 0
+    for args in ((2, 4, 8, 48, 3), (2, 4, 8, 32, 0), (2, 4, 8, 32, 257), (-1, 4, 8, 32, 1)):
+        assert pkg.attn_splitkv_workspace_size(*args)[0] == pkg.ATTN_ERR_INVALID_ARG
+
+
+W = 0x100000  # fake workspace address, far from the other fake pointers
+
+
+def skv(q=Q, k=K, v=V, o=O, lse=L, B=1, H=2, Sq=8, Skv=64, d=32, causal=0, scale=0.0,
+        dtype=pkg.ATTN_F32, n_splits=2, ws=W, ws_bytes=1 << 20):
+    return pkg.attn_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, dtype,
+                                n_splits, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(n_splits=0), dict(n_splits=257), dict(ws=None), dict(ws=W + 8),
+    dict(ws_bytes=4 * 2 * 2 * 8 * 33 - 4),   # one float short
+    dict(ws=Q), dict(ws=O - 64),               # workspace overlaps q / o
+    dict(d=48), dict(dtype=9), dict(causal=3), dict(q=Q + 4), dict(Sq=524281),
+], ids=lambda kw: ",".join("%s=%s" % i for i in kw.items()))
+def test_splitkv_rejects_invalid_arguments(lib, kw):
+    assert skv(**kw) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def _no_gpu():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except Exception:  # pragma: no cover
+        return True
+
+
+def test_splitkv_accepts_every_width_and_empty_problems(lib):
+    # Valid arguments pass validation and then stop at the device check.  The
+    # fake addresses must never reach a kernel, so this part runs only on a
+    # host without a GPU.
+    if not _no_gpu():
+        pytest.skip("valid calls with fake pointers would launch on this host")
+    for dt in (pkg.ATTN_F32, pkg.ATTN_BF16, pkg.ATTN_F16):
+        for d in (16, 32, 64, 128):
+            assert skv(d=d, dtype=dt) == pkg.ATTN_ERR_UNSUPPORTED_DEVICE
+    assert skv(B=0, q=None, k=None, v=None, o=None, lse=None, ws=None) == pkg.ATTN_OK
+    assert skv(Sq=0, ws=None) == pkg.ATTN_OK
+
+
+def merge_call(po=0x200000, pl=0x300000, n=3, rows=16, d=32, o=0x400000, lse=0x500000,
+               out=pkg.ATTN_F32):
+    return pkg.attn_merge(po, pl, n, rows, d, o, lse, out, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(n=0), dict(rows=-1), dict(d=0), dict(out=pkg.ATTN_BF16_OUT_F32), dict(out=7),
+    dict(po=None), dict(pl=None), dict(o=None), dict(po=0x200002), dict(o=0x400001),
+    dict(o=0x200000 + 64),          # output inside the partial outputs
+    dict(lse=0x300000),             # lse on top of the partial lse
+], ids=lambda kw: ",".join("%s=%s" % i for i in kw.items()))
+def test_merge_rejects_invalid_arguments(lib, kw):
+    assert merge_call(**kw) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_merge_empty_rows_is_noop(lib):
+    assert merge_call(rows=0, po=None, pl=None, o=None, lse=None) == pkg.ATTN_OK
