@@ -42,8 +42,18 @@ CONFIGS = {
     "b2_h4_s512_d64_f32": (2, 4, 512, 512, 64, False, "f32", "normal"),
     "b1_h32_s8192_d128_bf16_causal": (1, 32, 8192, 8192, 128, True, "bf16", "normal"),
     "b1_h64_s32768_d128_bf16_causal": (1, 64, 32768, 32768, 128, True, "bf16", "normal"),
+    # decode: one query row per head against a long key sequence, split-KV path
+    "b4_h32_q1_kv32768_d128_bf16_decode": (4, 32, 1, 32768, 128, False, "bf16", "normal"),
 }
+SPLITKV = {"b4_h32_q1_kv32768_d128_bf16_decode"}
 DEFAULT = "b1_h32_s8192_d128_bf16_causal"
+
+
+def compulsory_bytes(cfg):
+    """Bytes every implementation must move: Q, K, V read, O and LSE written."""
+    B, H, Sq, Skv, d, causal, dt, _ = cfg
+    e = 4 if dt == "f32" else 2
+    return B * H * (Sq * d * e * 2 + 2 * Skv * d * e + Sq * 4)
 
 
 def flops(B, H, Sq, Skv, d, causal):
@@ -64,9 +74,11 @@ def load_peaks():
                 "source": "fallback"}
 
 
-def kernel_source_hash():
+def kernel_source_hash(config_name=DEFAULT):
+    """Hash of the source files of the dominant kernel of a workload."""
+    files = ("attn_splitkv.cu",) if config_name in SPLITKV else ("attn_tc.cu", "sm100_ptx.cuh")
     h = hashlib.sha256()
-    for f in ("attn_tc.cu", "sm100_ptx.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "online_softmax_forward_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -77,7 +89,7 @@ def profiled_traffic(config_name):
     source (profiles/*.md line 'traffic_bytes_per_launch: N kernel_sha: H
     config: C'); None if absent or taken on another kernel version."""
     pdir = os.path.join(ROOT, "profiles")
-    want = kernel_source_hash()
+    want = kernel_source_hash(config_name)
     if not os.path.isdir(pdir):
         return None
     pat = re.compile(r"traffic_bytes_per_launch:\s*(\d+)\s+kernel_sha:\s*(\w+)\s+config:\s*(\S+)")
@@ -192,12 +204,24 @@ def run_gpu(args, rank, world, local_rank):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
-
-    def launch():
-        st = pkg.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                          lse.data_ptr(), B, H, Sq, Skv, d, int(causal), 0.0, code, sh)
+    splitkv = args.config in SPLITKV
+    n_splits, ws = 0, None
+    if splitkv:
+        st, n_splits, ws_bytes = pkg.attn_splitkv_plan(B, H, Sq, Skv, d, code)
         if st != pkg.ATTN_OK:
-            raise pkg.AttnError(st, "attn_fwd")
+            raise pkg.AttnError(st, "attn_splitkv_plan")
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+    def launch(qq=q, kk=k, vv=v):
+        if splitkv:
+            st = pkg.attn_fwd_splitkv(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr(), B, H, Sq, Skv, d, int(causal), 0.0, code,
+                                      n_splits, ws.data_ptr(), ws.numel(), sh)
+        else:
+            st = pkg.attn_fwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), B, H, Sq, Skv, d, int(causal), 0.0, code, sh)
+        if st != pkg.ATTN_OK:
+            raise pkg.AttnError(st, "attn_fwd_splitkv" if splitkv else "attn_fwd")
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -243,12 +267,20 @@ def run_gpu(args, rank, world, local_rank):
             flush.fill_(i & 0xFF)
             stream.synchronize()
             t0 = time.perf_counter()
-            st = pkg.attn_fwd_staged(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), oh.data_ptr(),
-                                     lh.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                                     o.data_ptr(), lse.data_ptr(), B, H, Sq, Skv, d, int(causal),
-                                     0.0, code, sh)
-            if st != pkg.ATTN_OK:
-                raise pkg.AttnError(st, "attn_fwd_staged")
+            if splitkv:  # host -> device copies, the split-KV call, device -> host copies
+                for dst, src_ in ((dq, qh), (dk, kh), (dv, vh)):
+                    dst.copy_(src_, non_blocking=True)
+                launch(dq, dk, dv)
+                oh.copy_(o, non_blocking=True)
+                lh.copy_(lse, non_blocking=True)
+            else:
+                st = pkg.attn_fwd_staged(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(),
+                                         oh.data_ptr(), lh.data_ptr(), dq.data_ptr(),
+                                         dk.data_ptr(), dv.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), B, H, Sq, Skv, d, int(causal), 0.0,
+                                         code, sh)
+                if st != pkg.ATTN_OK:
+                    raise pkg.AttnError(st, "attn_fwd_staged")
             stream.synchronize()
             if i >= args.warmup:
                 e2e_times.append(time.perf_counter() - t0)
@@ -259,7 +291,8 @@ def run_gpu(args, rank, world, local_rank):
     # max over ranks of the per-step device time
     ms_max, e2e_s = max_over_ranks([ms, sum(e2e_times) / len(e2e_times)], world, dev)
     return dict(ms=ms_max, flops=f, times=times, wall=wall, clocks=clocks, e2e_s=e2e_s,
-                h2d=h2d, d2h=d2h, cfg=cfg)
+                h2d=h2d, d2h=d2h, cfg=cfg, launches_per_step=2 if splitkv else 1,
+                n_splits=n_splits)
 
 
 def cpu_baseline(cfg, target_s=12.0):
@@ -352,6 +385,7 @@ def main(argv=None):
     B, H, Sq, Skv, d, causal, dt, _ = cfg
     peaks = load_peaks()
     config = {"workload": args.config, "B": B, "H": H, "Sq": Sq, "Skv": Skv, "d": d,
+              "path": "split-KV (attn_fwd_splitkv)" if args.config in SPLITKV else "attn_fwd",
               "causal": causal, "inputs": "iid standard normal, seeded" if cfg[7] == "normal"
               else "iid uniform(-0.8,0.8), random.Random(42)",
               "l2": "flushed between steps (256 MiB fill outside the kernel events)",
@@ -382,14 +416,13 @@ def main(argv=None):
         return 0
     tflops = r["flops"] / (r["ms"] * 1e-3) / 1e12
     value = world * tflops
-    if cfg[6] == "bf16":
+    if cfg[6] == "bf16" and args.config not in SPLITKV:
         peak, unit, bound = peaks["bf16_tflops"], "TFLOP/s", "tensor"
         achieved = tflops
     else:
-        # fp32 small cases: report against HBM (compulsory bytes)
-        comp = 4 * (B * H * Sq * d * 2 + B * H * Skv * d * 2) + 4 * B * H * Sq
+        # decode and the small fp32 cases: compulsory bytes against HBM
         peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
-        achieved = comp / (r["ms"] * 1e-3) / 1e9
+        achieved = compulsory_bytes(cfg) / (r["ms"] * 1e-3) / 1e9
     traffic = profiled_traffic(args.config)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -403,7 +436,7 @@ def main(argv=None):
                                                        if bound == "tensor" else " copy GB/s")},
         "e2e": {"value": world * r["flops"] / r["e2e_s"] / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * r["launches_per_step"],
         "clocks": r["clocks"],
         "step_ms_min": min(r["times"]), "step_ms_max": max(r["times"]),
     }

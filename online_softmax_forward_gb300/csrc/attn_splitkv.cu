@@ -18,7 +18,8 @@
 //
 // Partial kernel: CTA (bh, split, block of RB query rows).  Each warp walks
 // its own 32-key tiles of the split (tiles warp, warp + W, ...), staged in
-// shared memory with 16-byte cp.async in a two-stage ring per warp, and keeps
+// shared memory with 16-byte cp.async (each instruction of the warp copies
+// 512 contiguous bytes) in a ring of kStages tiles per warp, and keeps
 // its own running max m, normaliser l and accumulator a for every row:
 // lane = key for the scores (q pre-multiplied by scale * log2 e), warp
 // shuffles for the tile max and sum, lanes over the head dimension for P.V.
@@ -36,7 +37,7 @@ namespace attn {
 namespace {
 
 constexpr int kTileKeys = 32;  // keys per warp tile: one per lane
-constexpr size_t kSkvSmemLimit = 200 * 1024;
+constexpr size_t kSkvSmemLimit = 227 * 1024;
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -136,8 +137,10 @@ struct SkvCfg {
     static constexpr int kRow = D * (int)sizeof(T) + 16;
     static constexpr int kTile = kTileKeys * kRow;  // one K or V tile
     static constexpr int kStage = 2 * kTile;        // K and V
-    static constexpr int kWarpRing = 2 * kStage;    // two stages
-    static constexpr int kWarps = (4 * kWarpRing <= 160 * 1024) ? 4 : 2;
+    // 3 stages per warp keep two tiles in flight while one is computed
+    static constexpr int kStages = 3;
+    static constexpr int kWarpRing = kStages * kStage;
+    static constexpr int kWarps = (4 * kWarpRing <= 210 * 1024) ? 4 : 2;
     static_assert((kRow / 16) % 2 == 1, "row stride must be an odd number of 16-byte units");
 };
 
@@ -189,29 +192,39 @@ splitkv_partial_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
         for (int u = 0; u < CPL; ++u) acc[i][u] = 0.f;
     }
 
-    // K and V rows of this lane's key of tile `tile` into ring stage `stage`;
-    // keys past the range are zero-filled (never read from global memory).
+    // K and V rows of tile `tile` into ring stage `stage`: 16-byte piece g of
+    // the tile (row g / kChunks, chunk g % kChunks) is copied by lane g % 32,
+    // so each instruction of the warp reads 512 contiguous bytes.  Keys past
+    // the range are zero-filled (never read from global memory).
     auto issue = [&](int tile, int stage) {
-        const int j = kb + tile * kTileKeys + lane;
-        const bool in = j < ke;
-        const size_t row = (size_t)(in ? j : kb) * D;
-        const uint32_t kdst = smem_u32(ring + stage * C::kStage + lane * C::kRow);
+        const uint32_t kbase = smem_u32(ring + stage * C::kStage);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c) {
-            cp_async16(kdst + c * 16, kg + row + c * C::kElems16, in ? 16 : 0);
-            cp_async16(kdst + C::kTile + c * 16, vg + row + c * C::kElems16, in ? 16 : 0);
+        for (int it2 = 0; it2 < C::kChunks; ++it2) {
+            const int g = it2 * 32 + lane;
+            const int r = g / C::kChunks, c = g % C::kChunks;
+            const int j = kb + tile * kTileKeys + r;
+            const bool in = j < ke;
+            const size_t src = (size_t)(in ? j : kb) * D + c * C::kElems16;
+            const uint32_t dst = kbase + r * C::kRow + c * 16;
+            cp_async16(dst, kg + src, in ? 16 : 0);
+            cp_async16(dst + C::kTile, vg + src, in ? 16 : 0);
         }
     };
 
-    if (warp < ntiles) issue(warp, 0);
-    cp_async_commit();
+    // prologue: the first kStages - 1 tiles of this warp
+#pragma unroll
+    for (int s = 0; s < C::kStages - 1; ++s) {
+        if (warp + s * W < ntiles) issue(warp + s * W, s);
+        cp_async_commit();
+    }
     int it = 0;
     for (int tile = warp; tile < ntiles; tile += W, ++it) {
-        const int stage = it & 1;
-        if (tile + W < ntiles) issue(tile + W, stage ^ 1);
+        const int stage = it % C::kStages;
+        const int ahead = tile + (C::kStages - 1) * W;
+        if (ahead < ntiles) issue(ahead, (it + C::kStages - 1) % C::kStages);
         cp_async_commit();
-        cp_async_wait<1>();  // this tile's copies have landed
-        __syncwarp();
+        cp_async_wait<C::kStages - 1>();  // this tile's copies have landed
+        __syncwarp();  // ... for every lane, which also copied other lanes' rows
         const uint8_t *Kt = ring + stage * C::kStage;
         const uint8_t *Vt = Kt + C::kTile;
         const int j = kb + tile * kTileKeys + lane;
@@ -419,7 +432,40 @@ int launch_partial_d(const void *q, const void *k, const void *v, float *po, flo
 
 int warps_for(int d, int dtype) {
     const size_t row = (size_t)d * elem_bytes_in(dtype) + 16;
-    return 4 * 4 * kTileKeys * row <= 160 * 1024 ? 4 : 2;
+    return 4 * 3 * 2 * kTileKeys * row <= 210 * 1024 ? 4 : 2;
+}
+
+// Resident CTAs per SM of the partial kernel for this problem (>= 1).
+template <int D, typename T, int RB>
+int occupancy_t() {
+    constexpr size_t smem = skv_smem_bytes<D, T, RB>();
+    auto kern = splitkv_partial_kernel<D, T, RB>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, SkvCfg<D, T>::kWarps * 32,
+                                                      smem) != cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+template <int D, typename T>
+int occupancy_rb(int Sq) {
+    return Sq <= 1 ? occupancy_t<D, T, 1>() : occupancy_t<D, T, kSplitRowBlock>();
+}
+template <typename T>
+int occupancy_d(int d, int Sq) {
+    switch (d) {
+    case 16: return occupancy_rb<16, T>(Sq);
+    case 32: return occupancy_rb<32, T>(Sq);
+    case 64: return occupancy_rb<64, T>(Sq);
+    default: return occupancy_rb<128, T>(Sq);
+    }
+}
+int splitkv_occupancy(const Problem &p) {
+    if (p.dtype == ATTN_F32) return occupancy_d<float>(p.d, p.Sq);
+    if (p.dtype == ATTN_BF16 || p.dtype == ATTN_BF16_OUT_F32)
+        return occupancy_d<__nv_bfloat16>(p.d, p.Sq);
+    return occupancy_d<__half>(p.d, p.Sq);
 }
 
 }  // namespace
@@ -436,19 +482,33 @@ void splitkv_chunking(int Skv, int n_splits, int *chunk, int *n_eff) {
     *n_eff = Skv > 0 ? (Skv + c - 1) / c : 1;
 }
 
+// The split count with the smallest estimated time: waves of CTAs over the
+// GPU's resident slots times the key tiles each warp walks, plus a small
+// charge per split for the merge; at least two tiles per warp in a split.
 int splitkv_choose(const Problem &p, int sms) {
     const int64_t rows_blocks = (p.Sq + splitkv_row_block(p.Sq) - 1) / splitkv_row_block(p.Sq);
     const int64_t base = p.bh() * rows_blocks;
-    const int64_t target = 4LL * (sms > 0 ? sms : 1);
-    int64_t n = (target + base - 1) / base;
-    // at least two tiles per warp in every split
-    const int64_t min_keys = 2LL * warps_for(p.d, p.dtype) * kTileKeys;
+    const int W = warps_for(p.d, p.dtype);
+    const int64_t slots = (int64_t)(sms > 0 ? sms : 1) * splitkv_occupancy(p);
+    const int64_t min_keys = 2LL * W * kTileKeys;
     int64_t max_n = (p.Skv + min_keys - 1) / min_keys;
     if (max_n < 1) max_n = 1;
-    if (n > max_n) n = max_n;
-    if (n > kMaxSplits) n = kMaxSplits;
-    if (n < 1) n = 1;
-    return (int)n;
+    if (max_n > kMaxSplits) max_n = kMaxSplits;
+    int best = 1;
+    double best_cost = 1e300;
+    for (int n = 1; n <= max_n; ++n) {
+        int chunk = 0, n_eff = 0;
+        splitkv_chunking(p.Skv, n, &chunk, &n_eff);
+        if (n_eff != n) continue;  // the same chunking as a smaller count
+        const int64_t waves = (base * n + slots - 1) / slots;
+        const int64_t tiles = ((chunk + kTileKeys - 1) / kTileKeys + W - 1) / W;
+        const double cost = (double)waves * (double)tiles + 0.02 * n;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = n;
+        }
+    }
+    return best;
 }
 
 int launch_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,

@@ -55,3 +55,15 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert rec["impl"] == "reference" and rec["unit"] == "TFLOP/s"
     assert rec["cpu_baseline"]["kind"] == "oracle"
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_compulsory_bytes_and_paths():
+    # decode: q, o (bf16), k, v (bf16) and lse (fp32)
+    cfg = bench.CONFIGS["b4_h32_q1_kv32768_d128_bf16_decode"]
+    B, H, Sq, Skv, d = 4, 32, 1, 32768, 128
+    assert bench.compulsory_bytes(cfg) == B * H * (2 * Sq * d * 2 + 2 * Skv * d * 2 + Sq * 4)
+    assert "b4_h32_q1_kv32768_d128_bf16_decode" in bench.SPLITKV
+    assert bench.DEFAULT not in bench.SPLITKV
+    # the traffic record is keyed by the source of the workload's dominant kernel
+    assert bench.kernel_source_hash(bench.DEFAULT) != \
+        bench.kernel_source_hash("b4_h32_q1_kv32768_d128_bf16_decode")
