@@ -64,7 +64,8 @@ typedef enum attn_status {
     ATTN_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not compute capability 10.3 */
     ATTN_ERR_LAUNCH = 3,             /* a CUDA launch or copy failed */
     ATTN_ERR_TIMEOUT = 4,            /* a kernel's bounded wait expired (see attn_check_status) */
-    ATTN_ERR_CUDA = 5                /* another CUDA runtime/driver error */
+    ATTN_ERR_CUDA = 5,               /* another CUDA runtime/driver error */
+    ATTN_ERR_SCRATCH_LIMIT = 6       /* attn_fwd_splitkv_noalloc: problem exceeds its fixed scratch */
 } attn_status;
 
 typedef enum attn_dtype {
@@ -180,6 +181,37 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float
                      int B, int H, int Sq, int Skv, int d, int causal, float scale,
                      int dtype, int n_splits, void *workspace, size_t workspace_bytes,
                      void *stream);
+
+/*
+ * attn_fwd_splitkv_noalloc -- attn_fwd_splitkv for callers that must not
+ * allocate memory.  No passage of the source pages corresponds to it: it is
+ * an interface for code that cannot call cudaMalloc, for example code
+ * running inside a custom allocator or a memory-pool callback, a runtime
+ * that forbids allocation on its serving path, or a caller whose memory
+ * budget is fixed in advance.
+ *
+ * Instead of a caller-provided workspace it uses a scratch array of
+ * ATTN_NOALLOC_SCRATCH_BYTES (8 MiB) that is part of the library's device
+ * image: every GPU that loads the library holds it until the process exits.
+ * The call itself allocates nothing and calls no allocating routine.
+ *   - Size limit: the problem must fit, i.e.
+ *     4 * n_splits * B * H * Sq * (d + 1) <= ATTN_NOALLOC_SCRATCH_BYTES
+ *     (see attn_splitkv_workspace_size); otherwise ATTN_ERR_SCRATCH_LIMIT is
+ *     returned before anything is launched.
+ *   - First call on a device: it looks up the array's device address once
+ *     for that device (with that device current).  Make that first call
+ *     before capturing a stream.
+ *   - Sharing: every call uses the same array, which keeps the contents of
+ *     the last call.  Nothing in it needs to start at zero (each partial
+ *     result is written before it is read), but calls that overlap on the GPU
+ *     (different streams, or different host threads without ordering) race
+ *     on it: order them, e.g. on one stream.
+ * Other arguments, results and errors as attn_fwd_splitkv.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int Sq, int Skv, int d, int causal, float scale,
+                             int dtype, int n_splits, void *stream);
 
 /*
  * attn_merge -- combines partial attention results of the same query rows

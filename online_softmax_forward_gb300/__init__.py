@@ -16,12 +16,13 @@ import os
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED_DEVICE", "ATTN_ERR_LAUNCH",
-    "ATTN_ERR_TIMEOUT", "ATTN_ERR_CUDA",
+    "ATTN_ERR_TIMEOUT", "ATTN_ERR_CUDA", "ATTN_ERR_SCRATCH_LIMIT", "NOALLOC_SCRATCH_BYTES",
     "ATTN_F32", "ATTN_BF16", "ATTN_F16", "ATTN_BF16_OUT_F32", "ATTN_F16_OUT_F32",
     "AttnError", "library_path", "load_library", "exported_symbols",
     "attn_fwd", "attn_validate", "attn_fwd_f32_blocked", "attn_fwd_staged",
     "attn_check_status", "attn_strerror", "attn_abi_version", "attn_test_set_hook",
     "attn_splitkv_workspace_size", "attn_splitkv_plan", "attn_fwd_splitkv", "attn_merge",
+    "attn_fwd_splitkv_noalloc",
     "attention", "attention_f32_blocked", "attention_splitkv", "merge", "dtype_code",
 ]
 
@@ -31,6 +32,8 @@ ATTN_ERR_UNSUPPORTED_DEVICE = 2
 ATTN_ERR_LAUNCH = 3
 ATTN_ERR_TIMEOUT = 4
 ATTN_ERR_CUDA = 5
+ATTN_ERR_SCRATCH_LIMIT = 6
+NOALLOC_SCRATCH_BYTES = 8 << 20  # the fixed scratch of attn_fwd_splitkv_noalloc
 
 ATTN_F32 = 0
 ATTN_BF16 = 1
@@ -61,6 +64,8 @@ _SIGS = [
     ("attn_fwd_splitkv", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P,
                               ctypes.c_size_t, _P]),
     ("attn_merge", _I, [_P, _P, _I, ctypes.c_int64, _I, _P, _P, _I, _P]),
+    ("attn_fwd_splitkv_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                                      _P]),
 ]
 
 
@@ -169,6 +174,15 @@ def attn_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, dtype, n_
     return load_library().attn_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Skv, d, int(causal),
                                            float(scale), dtype, int(n_splits), workspace,
                                            int(workspace_bytes), stream)
+
+
+def attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, dtype, n_splits,
+                             stream):
+    """attn_fwd_splitkv with the library's fixed device scratch instead of a
+    workspace: for callers that cannot allocate (see include/attn.h)."""
+    return load_library().attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Sq, Skv, d,
+                                                   int(causal), float(scale), dtype,
+                                                   int(n_splits), stream)
 
 
 def attn_merge(o_parts, lse_parts, n_parts, rows, d, o, lse, out_dtype, stream):

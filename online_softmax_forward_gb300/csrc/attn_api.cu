@@ -168,6 +168,7 @@ const char *attn_strerror(int status) {
     case ATTN_ERR_LAUNCH: return "kernel launch or copy failed";
     case ATTN_ERR_TIMEOUT: return "a kernel gave up a bounded wait; its output is incomplete";
     case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_SCRATCH_LIMIT: return "the problem needs more scratch than the fixed device array of attn_fwd_splitkv_noalloc holds";
     default: return "unknown status";
     }
 }
@@ -289,6 +290,29 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float
     if (st != ATTN_OK) return st;
     if (Skv == 0) return launch_empty_keys(o, lse, p, (cudaStream_t)stream);
     float *part_o = (float *)workspace;
+    float *part_lse = part_o + (size_t)n_splits * p.bh() * Sq * d;
+    return launch_splitkv(q, k, v, o, lse, p, n_splits, part_o, part_lse, (cudaStream_t)stream);
+}
+
+int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int Sq, int Skv, int d, int causal, float scale,
+                             int dtype, int n_splits, void *stream) {
+    Problem p;
+    int st = validate(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, dtype, &p, true);
+    if (st != ATTN_OK) return st;
+    if (n_splits < 1 || n_splits > kMaxSplits || Sq > kMaxSplitRows) return ATTN_ERR_INVALID_ARG;
+    if (p.bh() == 0 || Sq == 0) return ATTN_OK;
+    size_t need = 0;
+    if (!splitkv_bytes(p.bh(), Sq, d, n_splits, &need) || need > kNoAllocScratchBytes)
+        return ATTN_ERR_SCRATCH_LIMIT;
+    st = check_device();
+    if (st != ATTN_OK) return st;
+    if (Skv == 0) return launch_empty_keys(o, lse, p, (cudaStream_t)stream);
+    void *scratch = nullptr;
+    st = noalloc_scratch_ptr(&scratch);
+    if (st != ATTN_OK) return st;
+    // every partial result the merge reads is written first: nothing to clear
+    float *part_o = (float *)scratch;
     float *part_lse = part_o + (size_t)n_splits * p.bh() * Sq * d;
     return launch_splitkv(q, k, v, o, lse, p, n_splits, part_o, part_lse, (cudaStream_t)stream);
 }

@@ -48,6 +48,12 @@ int launch_splitkv(const void *q, const void *k, const void *v, void *o, float *
 int launch_merge(const float *po, const float *pl, int n_parts, int64_t rows, int d, void *o,
                  float *lse, int out_dtype, cudaStream_t stream);
 
+// Fixed device scratch of attn_fwd_splitkv_noalloc (attn_splitkv.cu): its
+// size, and its device address on the current device (looked up once per
+// device).
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
+int noalloc_scratch_ptr(void **ptr);
+
 // Writes o = 0 and lse = -inf (Skv == 0).
 int launch_empty_keys(void *o, float *lse, const Problem &p, cudaStream_t stream);
 

@@ -29,11 +29,19 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <mutex>
 #include <stdint.h>
 
 #include "attn_internal.h"
 
 namespace attn {
+
+// Scratch of attn_fwd_splitkv_noalloc: a fixed array in device memory, so
+// that the call needs no allocation.  Every device that loads the library
+// holds it until the process exits.  Host code cannot use the name as an
+// address; the address is looked up per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int kTileKeys = 32;  // keys per warp tile: one per lane
@@ -471,6 +479,29 @@ int splitkv_occupancy(const Problem &p) {
 }  // namespace
 
 int splitkv_row_block(int Sq) { return Sq <= 1 ? 1 : kSplitRowBlock; }
+
+// Device address of g_noalloc_scratch on the current device, looked up with
+// cudaGetSymbolAddress the first time a device asks and cached after that.
+int noalloc_scratch_ptr(void **ptr) {
+    constexpr int kMaxDev = 64;
+    static std::mutex mu;
+    static void *addr[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+                return ATTN_ERR_UNSUPPORTED_DEVICE;
+            return ATTN_ERR_CUDA;
+        }
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return ATTN_OK;
+}
 
 // Keys per split (a multiple of 32) and the number of non-empty splits for a
 // requested split count.
