@@ -225,6 +225,7 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *
  * A part with lse = -inf (no visible key) contributes nothing; a row whose
  * parts are all -inf gets o = 0 and lse = -inf.
  *
+ *   n_parts    1 .. 4096;  rows 0 .. 2^31 - 1;  d >= 1
  *   o_parts    [n_parts][rows][d] fp32, device memory
  *   lse_parts  [n_parts][rows]    fp32, natural log
  *   o          [rows][d] of out_dtype: ATTN_F32, ATTN_BF16 or ATTN_F16

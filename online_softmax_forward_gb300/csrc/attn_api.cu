@@ -319,7 +319,8 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *
 
 int attn_merge(const float *o_parts, const float *lse_parts, int n_parts, int64_t rows, int d,
                void *o, float *lse, int out_dtype, void *stream) {
-    if (n_parts < 1 || rows < 0 || d < 1) return ATTN_ERR_INVALID_ARG;
+    if (n_parts < 1 || n_parts > 4096 || rows < 0 || rows > INT32_MAX || d < 1)
+        return ATTN_ERR_INVALID_ARG;
     if (out_dtype != ATTN_F32 && out_dtype != ATTN_BF16 && out_dtype != ATTN_F16)
         return ATTN_ERR_INVALID_ARG;
     if (rows == 0) return ATTN_OK;

@@ -355,50 +355,70 @@ splitkv_partial_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
     }
 }
 
-// One warp per row: merges n_parts partial results [n_parts][rows][d] /
-// [n_parts][rows] into o [rows][d] and lse [rows].
+// One CTA of kMergeThreads per row: merges n_parts partial results
+// [n_parts][rows][d] / [n_parts][rows] into o [rows][d] and lse [rows].  The
+// weights exp(lse_p - M) are computed once into shared memory; each thread
+// then sums its columns over the parts.
+constexpr int kMergeThreads = 128;
+
+__device__ __forceinline__ float block_reduce(float x, float *red, bool is_max) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    x = is_max ? warp_max(x) : warp_sum(x);
+    __syncthreads();  // red may still be read by a previous reduction
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < kMergeThreads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+    return r;
+}
+
 template <typename TO>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kMergeThreads)
 merge_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_parts,
              int64_t rows, int d, TO *__restrict__ o, float *__restrict__ lse) {
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    float M = -INFINITY;
-    for (int p = lane; p < n_parts; p += 32) M = fmaxf(M, pl[(int64_t)p * rows + row]);
-    M = warp_max(M);
+    extern __shared__ float wts[];  // [n_parts]
+    __shared__ float red[kMergeThreads / 32];
+    const int64_t row = blockIdx.x;
     TO *orow = o + row * d;
+    float M = -INFINITY;
+    for (int p = threadIdx.x; p < n_parts; p += kMergeThreads)
+        M = fmaxf(M, pl[(int64_t)p * rows + row]);
+    M = block_reduce(M, red, true);
     if (M == -INFINITY) {  // no part saw a key: o = 0, lse = -inf
-        for (int c = lane; c < d; c += 32) orow[c] = from_f32<TO>(0.f);
-        if (lse && lane == 0) lse[row] = -INFINITY;
+        for (int c = threadIdx.x; c < d; c += kMergeThreads) orow[c] = from_f32<TO>(0.f);
+        if (lse && threadIdx.x == 0) lse[row] = -INFINITY;
         return;
     }
     float L = 0.f;
-    for (int p = lane; p < n_parts; p += 32) {
+    for (int p = threadIdx.x; p < n_parts; p += kMergeThreads) {
         const float lp = pl[(int64_t)p * rows + row];
-        if (lp != -INFINITY) L += expf(lp - M);
+        const float w = lp == -INFINITY ? 0.f : expf(lp - M);  // a part with no key weighs 0
+        wts[p] = w;
+        L += w;
     }
-    L = warp_sum(L);
+    L = block_reduce(L, red, false);  // also makes wts visible to every thread
     const float inv = 1.f / L;
-    for (int c = lane; c < d; c += 32) {
+    for (int c = threadIdx.x; c < d; c += kMergeThreads) {
         float a = 0.f;
+        const float *col = po + row * d + c;
+#pragma unroll 4
         for (int p = 0; p < n_parts; ++p) {
-            const float lp = pl[(int64_t)p * rows + row];
-            if (lp != -INFINITY) a = fmaf(expf(lp - M), po[((int64_t)p * rows + row) * d + c], a);
+            const float w = wts[p];
+            if (w != 0.f) a = fmaf(w, col[(int64_t)p * rows * d], a);
         }
         orow[c] = from_f32<TO>(a * inv);
     }
-    if (lse && lane == 0) lse[row] = M + logf(L);
+    if (lse && threadIdx.x == 0) lse[row] = M + logf(L);
 }
 
 template <typename TO>
 int launch_merge_t(const float *po, const float *pl, int n_parts, int64_t rows, int d, void *o,
                    float *lse, cudaStream_t stream) {
     if (rows == 0) return ATTN_OK;
-    const int64_t blocks = (rows + 7) / 8;
-    if (blocks > INT32_MAX) return ATTN_ERR_INVALID_ARG;
-    merge_kernel<TO><<<(unsigned)blocks, 256, 0, stream>>>(po, pl, n_parts, rows, d,
-                                                           reinterpret_cast<TO *>(o), lse);
+    if (rows > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+    merge_kernel<TO><<<(unsigned)rows, kMergeThreads, (size_t)n_parts * sizeof(float), stream>>>(
+        po, pl, n_parts, rows, d, reinterpret_cast<TO *>(o), lse);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 

@@ -161,7 +161,7 @@ def merge_call(po=0x200000, pl=0x300000, n=3, rows=16, d=32, o=0x400000, lse=0x5
 
 
 @pytest.mark.parametrize("kw", [
-    dict(n=0), dict(rows=-1), dict(d=0), dict(out=pkg.ATTN_BF16_OUT_F32), dict(out=7),
+    dict(n=0), dict(n=4097), dict(rows=-1), dict(rows=1 << 31), dict(d=0), dict(out=pkg.ATTN_BF16_OUT_F32), dict(out=7),
     dict(po=None), dict(pl=None), dict(o=None), dict(po=0x200002), dict(o=0x400001),
     dict(o=0x200000 + 64),          # output inside the partial outputs
     dict(lse=0x300000),             # lse on top of the partial lse
