@@ -44,6 +44,15 @@ CONFIGS = {
     "b1_h64_s32768_d128_bf16_causal": (1, 64, 32768, 32768, 128, True, "bf16", "normal"),
     # decode: one query row per head against a long key sequence, split-KV path
     "b4_h32_q1_kv32768_d128_bf16_decode": (4, 32, 1, 32768, 128, False, "bf16", "normal"),
+    # the access-model sweep of aiml.sh "verify-tiled-attention" (H=32, d=128, causal)
+    "b1_h32_s1024_d128_bf16_causal": (1, 32, 1024, 1024, 128, True, "bf16", "normal"),
+    "b1_h32_s4096_d128_bf16_causal": (1, 32, 4096, 4096, 128, True, "bf16", "normal"),
+    "b1_h32_s16384_d128_bf16_causal": (1, 32, 16384, 16384, 128, True, "bf16", "normal"),
+    "b1_h32_s32768_d128_bf16_causal": (1, 32, 32768, 32768, 128, True, "bf16", "normal"),
+    # other variants of the tensor-core kernel
+    "b1_h32_s8192_d128_fp16_causal": (1, 32, 8192, 8192, 128, True, "f16", "normal"),
+    "b1_h64_s8192_d64_bf16_causal": (1, 64, 8192, 8192, 64, True, "bf16", "normal"),
+    "b1_h32_s8192_d128_bf16_full": (1, 32, 8192, 8192, 128, False, "bf16", "normal"),
 }
 SPLITKV = {"b4_h32_q1_kv32768_d128_bf16_decode"}
 DEFAULT = "b1_h32_s8192_d128_bf16_causal"
@@ -167,7 +176,7 @@ def make_inputs(cfg, device, seed=0):
     import torch
     import qkv_inputs
     B, H, Sq, Skv, d, causal, dt, family = cfg
-    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}[dt]
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dt]
     if family == "uniform":
         q, k, v = (torch.from_numpy(a) for a in qkv_inputs.uniform_qkv(B, H, Sq, Skv, d, 42))
         return tuple(t.to(tdt).to(device) for t in (q, k, v))
@@ -176,7 +185,7 @@ def make_inputs(cfg, device, seed=0):
 
 def dtype_code(cfg):
     import online_softmax_forward_gb300 as pkg
-    return pkg.ATTN_F32 if cfg[6] == "f32" else pkg.ATTN_BF16
+    return {"f32": pkg.ATTN_F32, "bf16": pkg.ATTN_BF16, "f16": pkg.ATTN_F16}[cfg[6]]
 
 
 # ------------------------------------------------------------------ our arm
@@ -198,7 +207,7 @@ def run_gpu(args, rank, world, local_rank):
     B, H, Sq, Skv, d, causal, dt, _ = cfg
     code = dtype_code(cfg)
     q, k, v = make_inputs(cfg, dev, seed=rank)
-    odt = torch.float32 if dt == "f32" else torch.bfloat16
+    odt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dt]
     o = torch.empty((B, H, Sq, d), dtype=odt, device=dev)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -309,7 +318,8 @@ def cpu_baseline(cfg, target_s=12.0):
     else:
         # the heads sampled below only: draw the full tensors for the first head
         q, k, v = qkv_inputs.normal_qkv(1, 1, Sq, Skv, d, 0,
-                                        dtype=torch.bfloat16 if dt == "bf16" else None)
+                                        dtype={"bf16": torch.bfloat16,
+                                               "f16": torch.float16}.get(dt))
     qh, kh, vh = (t.reshape(-1, t.shape[-2], d)[:1] for t in (q, k, v))
     off = Skv - Sq
     nthreads = os.cpu_count() or 1
@@ -416,7 +426,8 @@ def main(argv=None):
         return 0
     tflops = r["flops"] / (r["ms"] * 1e-3) / 1e12
     value = world * tflops
-    if cfg[6] == "bf16" and args.config not in SPLITKV:
+    if cfg[6] in ("bf16", "f16") and args.config not in SPLITKV:
+        # fp16 and bf16 share the dense tensor-core rate: the bf16 measured peak serves both
         peak, unit, bound = peaks["bf16_tflops"], "TFLOP/s", "tensor"
         achieved = tflops
     else:
@@ -429,7 +440,8 @@ def main(argv=None):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dt, "data": "synthetic", "config": config,
-        "pct_of_dense_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"] if dt == "bf16" else None,
+        "pct_of_dense_bf16_peak": (100.0 * tflops / peaks["bf16_tflops"]
+                                   if dt in ("bf16", "f16") else None),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peaks["source"] + (" burst bf16 (kernel timed alone)"
