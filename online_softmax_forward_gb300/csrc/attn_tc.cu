@@ -109,6 +109,7 @@ struct TcParams {
     int *status;
     int BH, Sq, Skv, causal;
     int nqb;      // units per (batch, head): ceil(Sq / 256)
+    int hg;       // (batch, head) slices per schedule group (K/V of a group fit in L2)
     int n_units;  // BH * nqb
     float scale_log2;  // scale * log2(e)
     int out_f32;       // 1: o is fp32; 0: o has the input type
@@ -121,10 +122,18 @@ struct Unit {
     int nkv[2];
 };
 
+// Unit u of the schedule.  The (batch, head) slices are taken in groups of
+// hg whose K and V fit in L2 together; inside a group the units go level by
+// level, longest first for causal, and round-robin over the group's heads,
+// so the CTAs running at any time share the K/V of a few heads through L2.
 __device__ __forceinline__ Unit decode_unit(int u, const TcParams &p) {
     Unit r;
-    const int level = u / p.BH;
-    r.bh = u % p.BH;
+    const int per_group = p.hg * p.nqb;
+    const int g = u / per_group;
+    const int rem = u - g * per_group;
+    const int heads = min(p.hg, p.BH - g * p.hg);  // the last group may be smaller
+    const int level = rem / heads;
+    r.bh = g * p.hg + (rem - level * heads);
     const int qb = p.causal ? (p.nqb - 1 - level) : level;  // causal: longest first
     r.q0 = qb * 2 * BM;
     const int off = p.Skv - p.Sq;
@@ -748,6 +757,16 @@ int launch_typed(const void *q, const void *k, const void *v, void *o, float *ls
     p.Skv = pr.Skv;
     p.causal = pr.causal;
     p.nqb = (pr.Sq + 2 * BM - 1) / (2 * BM);
+    {
+        // heads per schedule group: all heads when their K and V fit in L2
+        // (about 160 MB with headroom); otherwise groups of about 64 MB
+        const int64_t kv_head = 2LL * pr.Skv * D * 2;
+        int64_t hg = BH;
+        if (kv_head > 0 && BH * kv_head > (160LL << 20)) hg = (int64_t)(64LL << 20) / kv_head;
+        if (hg < 1) hg = 1;
+        if (hg > BH) hg = BH;
+        p.hg = (int)hg;
+    }
     const int64_t n_units = BH * p.nqb;
     if (n_units > INT32_MAX) return ATTN_ERR_INVALID_ARG;
     p.n_units = (int)n_units;
