@@ -95,19 +95,20 @@ def test_rising_maximum_forces_rescale():
         assert_bf16_parity(o, lse, o_ref, lse_ref)
 
 
-def _sampled_parity(B, H, S, d, seed, n_random, heads=None, rows_per_head=None):
+def _sampled_parity(B, H, S, d, seed, n_random, heads=None, rows_per_head=None, causal=True):
     ensure_built()
     q, k, v = qkv_inputs.normal_qkv(B, H, S, S, d, seed=seed, dtype=torch.bfloat16)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    o32, lse = pkg.attention(qd, kd, vd, causal=True, out_dtype=torch.float32)
-    o16, lse16 = pkg.attention(qd, kd, vd, causal=True)
+    o32, lse = pkg.attention(qd, kd, vd, causal=causal, out_dtype=torch.float32)
+    o16, lse16 = pkg.attention(qd, kd, vd, causal=causal)
     torch.cuda.synchronize()
     assert pkg.attn_check_status(None) == pkg.ATTN_OK
     # properties of every row
     assert torch.isfinite(o32).all() and torch.isfinite(lse).all()
-    # row 0 sees key 0 only: its output is v[0] (exactly, once rounded to bf16)
-    assert torch.allclose(o32[:, :, 0], vd[:, :, 0].float(), rtol=1e-6, atol=0)
-    assert torch.equal(o16[:, :, 0], vd[:, :, 0])
+    if causal:
+        # row 0 sees key 0 only: its output is v[0] (exactly, once rounded to bf16)
+        assert torch.allclose(o32[:, :, 0], vd[:, :, 0].float(), rtol=1e-6, atol=0)
+        assert torch.equal(o16[:, :, 0], vd[:, :, 0])
     assert torch.equal(lse, lse16)
     vmin = vd.float().amin(dim=2, keepdim=True)
     vmax = vd.float().amax(dim=2, keepdim=True)
@@ -120,7 +121,7 @@ def _sampled_parity(B, H, S, d, seed, n_random, heads=None, rows_per_head=None):
     for bh in heads:
         rs = qkv_inputs.sample_rows(S, n_random, seed=1000 + bh)
         o_b, l_b = oracle.attention_rows(qh[bh:bh + 1], kh[bh:bh + 1], vh[bh:bh + 1],
-                                         [(0, i) for i in rs], causal=True)
+                                         [(0, i) for i in rs], causal=causal)
         rows += [(bh, i) for i in rs]
         o_parts.append(o_b)
         l_parts.append(l_b)
@@ -151,6 +152,16 @@ def test_b1_h64_s32768_d128_causal_sampled():
     mx, mean, n = _sampled_parity(1, 64, 32768, 128, seed=0, n_random=8,
                                   heads=(0, 21, 42, 63))
     print("c5 sampled rows %d: max %.3e mean %.3e" % (n, mx, mean))
+
+
+def test_grouped_schedule_noncausal_sampled():
+    """B=1, H=20, Sq=Skv=32768, d=128, non-causal: the K and V of all heads
+    (336 MB) exceed the L2, so the units are scheduled in head groups of 3
+    (the last group holds 2); sampled rows of heads in the first, a middle
+    and the last group against the oracle."""
+    mx, mean, n = _sampled_parity(1, 20, 32768, 128, seed=2, n_random=4, heads=(0, 10, 19),
+                                  causal=False)
+    print("grouped non-causal sampled rows %d: max %.3e mean %.3e" % (n, mx, mean))
 
 
 def test_deterministic():
