@@ -118,9 +118,17 @@ int attn_fwd_f32_blocked(const float *q, const float *k, const float *v,
  * attn_fwd_staged -- attn_fwd on HOST buffers: copies q, k, v from host memory
  * to the caller's device buffers dq, dk, dv, runs attn_fwd into do_ / dlse,
  * and copies o (and lse when both lse_host and dlse are non-NULL) back to
- * host memory, all enqueued on `stream` (one cudaMemcpyAsync per tensor).
+ * host memory (one cudaMemcpyAsync per tensor, or per tensor and chunk).
  * Host buffers should be pinned for the copies to be asynchronous.  The call
  * returns after enqueueing; synchronise the stream before reading o_host.
+ * Problems with at least 4 MiB of input are cut into 4 chunks of (batch,
+ * head) slices that run on two streams the library creates once per device:
+ * the copies of one chunk overlap the kernel of the other.  Those streams
+ * start after the work queued on `stream` and `stream` waits for them, so the
+ * call behaves as if everything ran on `stream`; concurrent staged calls on
+ * one device share the two streams.  After cudaDeviceReset the library's
+ * per-device state (these streams, cached device attributes, the status word
+ * address) is stale: do not call the library again in that process.
  * Sizes and dtype as attn_fwd; host pointers must not be NULL when their
  * tensor is non-empty.
  */

@@ -54,24 +54,70 @@ int cuda_to_status(cudaError_t e) {
     return ATTN_ERR_CUDA;
 }
 
-// The current device must be compute capability 10.3 (GB300).
+// The current device must be compute capability 10.3 (GB300).  The answer
+// is cached per device (1 = supported, 2 = not), so that small calls do not
+// pay for the attribute queries each time.
+int g_device_ok[kMaxDevices];
+
 int check_device() {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return ATTN_ERR_UNSUPPORTED_DEVICE;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int known = __atomic_load_n(&g_device_ok[dev], __ATOMIC_ACQUIRE);
+        if (known) return known == 1 ? ATTN_OK : ATTN_ERR_UNSUPPORTED_DEVICE;
+    }
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return ATTN_ERR_UNSUPPORTED_DEVICE;
-    if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED_DEVICE;
-    return ATTN_OK;
+    const bool ok = (major == 10 && minor == 3);
+    if (dev >= 0 && dev < kMaxDevices) __atomic_store_n(&g_device_ok[dev], ok ? 1 : 2, __ATOMIC_RELEASE);
+    return ok ? ATTN_OK : ATTN_ERR_UNSUPPORTED_DEVICE;
 }
+
+// (kernel, device) pairs whose shared-memory limit has been set.
+struct SmemDone {
+    const void *func;
+    int dev;
+    int bytes;
+};
+std::mutex g_smem_mu;
+SmemDone g_smem_done[256];
+int g_smem_n = 0;
+int g_sms[kMaxDevices];
 
 }  // namespace
 
 size_t elem_bytes_in(int dtype) { return dtype == ATTN_F32 ? 4 : 2; }
 size_t elem_bytes_out(int dtype) {
     return (dtype == ATTN_F32 || dtype == ATTN_BF16_OUT_F32 || dtype == ATTN_F16_OUT_F32) ? 4 : 2;
+}
+
+bool set_smem_limit_once(const void *func, int bytes) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lk(g_smem_mu);
+    for (int i = 0; i < g_smem_n; ++i)
+        if (g_smem_done[i].func == func && g_smem_done[i].dev == dev && g_smem_done[i].bytes >= bytes)
+            return true;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return false;
+    if (g_smem_n < 256) g_smem_done[g_smem_n++] = SmemDone{func, dev, bytes};
+    return true;
+}
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int n = __atomic_load_n(&g_sms[dev], __ATOMIC_ACQUIRE);
+        if (n > 0) return n;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) __atomic_store_n(&g_sms[dev], n, __ATOMIC_RELEASE);
+    return n;
 }
 
 int *status_word_device_ptr() {
@@ -84,6 +130,27 @@ int *status_word_device_ptr() {
         g_status_ptr[dev] = (int *)p;
     }
     return g_status_ptr[dev];
+}
+
+StagedStreams *staged_streams() {
+    static StagedStreams res[kMaxDevices];
+    static bool made[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!made[dev]) {
+        StagedStreams r;
+        for (int j = 0; j < 2; ++j) {
+            if (cudaStreamCreateWithFlags(&r.st[j], cudaStreamNonBlocking) != cudaSuccess ||
+                cudaEventCreateWithFlags(&r.done[j], cudaEventDisableTiming) != cudaSuccess)
+                return nullptr;
+        }
+        if (cudaEventCreateWithFlags(&r.start, cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+        res[dev] = r;
+        made[dev] = true;
+    }
+    return &res[dev];
 }
 
 int test_hook() { return g_hook; }
@@ -219,22 +286,60 @@ int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
     if (st != ATTN_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     const size_t ein = elem_bytes_in(dtype), eout = elem_bytes_out(dtype);
-    if (cudaMemcpyAsync(dq, q_host, nq * ein, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return ATTN_ERR_LAUNCH;
-    if (nkv > 0) {
-        if (cudaMemcpyAsync(dk, k_host, nkv * ein, cudaMemcpyHostToDevice, s) != cudaSuccess)
-            return ATTN_ERR_LAUNCH;
-        if (cudaMemcpyAsync(dv, v_host, nkv * ein, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    const int64_t BH = p.bh();
+    const size_t in_bytes = (nq + 2 * nkv) * ein;
+    const int nchunks = (BH >= 2 && in_bytes >= kStagedMinBytes)
+                            ? (int)(BH < kStagedChunks ? BH : kStagedChunks) : 1;
+    StagedStreams *res = nullptr;
+    if (nchunks > 1) {
+        res = staged_streams();
+        if (!res) return ATTN_ERR_CUDA;
+        // the chunks start after the work the caller has queued on `stream`
+        if (cudaEventRecord(res->start, s) != cudaSuccess ||
+            cudaStreamWaitEvent(res->st[0], res->start, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(res->st[1], res->start, 0) != cudaSuccess)
             return ATTN_ERR_LAUNCH;
     }
-    st = fwd_impl(dq, dk, dv, do_, dlse, p, s);
-    if (st != ATTN_OK) return st;
-    if (cudaMemcpyAsync(o_host, do_, nq * eout, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return ATTN_ERR_LAUNCH;
-    if (lse_host && dlse) {
-        if (cudaMemcpyAsync(lse_host, dlse, (size_t)p.bh() * Sq * 4, cudaMemcpyDeviceToHost,
-                            s) != cudaSuccess)
+    for (int i = 0; i < nchunks; ++i) {
+        // (batch, head) slices [b0, b1) on alternating streams: the copies of
+        // one chunk overlap the kernel and the copies of the other
+        const int64_t b0 = BH * i / nchunks, b1 = BH * (i + 1) / nchunks;
+        cudaStream_t cs = nchunks > 1 ? res->st[i & 1] : s;
+        const size_t oq = (size_t)b0 * Sq * d, okv = (size_t)b0 * Skv * d;
+        const size_t cq = (size_t)(b1 - b0) * Sq * d, ckv = (size_t)(b1 - b0) * Skv * d;
+        char *dqc = (char *)dq + oq * ein, *dkc = (char *)dk + okv * ein, *dvc = (char *)dv + okv * ein;
+        char *doc = (char *)do_ + oq * eout;
+        float *dlc = dlse ? dlse + (size_t)b0 * Sq : nullptr;
+        if (cudaMemcpyAsync(dqc, (const char *)q_host + oq * ein, cq * ein, cudaMemcpyHostToDevice,
+                            cs) != cudaSuccess)
             return ATTN_ERR_LAUNCH;
+        if (ckv > 0) {
+            if (cudaMemcpyAsync(dkc, (const char *)k_host + okv * ein, ckv * ein,
+                                cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+                cudaMemcpyAsync(dvc, (const char *)v_host + okv * ein, ckv * ein,
+                                cudaMemcpyHostToDevice, cs) != cudaSuccess)
+                return ATTN_ERR_LAUNCH;
+        }
+        Problem sub = p;
+        sub.B = 1;
+        sub.H = (int)(b1 - b0);
+        st = fwd_impl(dqc, dkc, dvc, doc, dlc, sub, cs);
+        if (st != ATTN_OK) return st;
+        if (cudaMemcpyAsync((char *)o_host + oq * eout, doc, cq * eout, cudaMemcpyDeviceToHost,
+                            cs) != cudaSuccess)
+            return ATTN_ERR_LAUNCH;
+        if (lse_host && dlse) {
+            if (cudaMemcpyAsync(lse_host + (size_t)b0 * Sq, dlc, (size_t)(b1 - b0) * Sq * 4,
+                                cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+                return ATTN_ERR_LAUNCH;
+        }
+    }
+    if (nchunks > 1) {
+        // the caller's stream continues once both chunk streams are done
+        for (int j = 0; j < 2; ++j)
+            if (cudaEventRecord(res->done[j], res->st[j]) != cudaSuccess ||
+                cudaStreamWaitEvent(s, res->done[j], 0) != cudaSuccess)
+                return ATTN_ERR_LAUNCH;
     }
     return ATTN_OK;
 }
@@ -254,10 +359,8 @@ int attn_splitkv_plan(int B, int H, int Sq, int Skv, int d, int dtype, int *n_sp
         return ATTN_ERR_INVALID_ARG;
     st = check_device();
     if (st != ATTN_OK) return st;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return ATTN_ERR_CUDA;
+    const int sms = device_sm_count();
+    if (sms <= 0) return ATTN_ERR_CUDA;
     p.B = B; p.H = H; p.Sq = Sq; p.Skv = Skv;
     *n_splits = splitkv_choose(p, sms);
     if (workspace_bytes)

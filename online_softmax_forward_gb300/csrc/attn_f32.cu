@@ -190,8 +190,7 @@ template <int D>
 int launch_d(const float *q, const float *k, const float *v, float *o, float *lse,
              const Problem &p, int bq, int bkv, cudaStream_t stream) {
     const size_t smem = f32_smem_bytes(D, bq, bkv);
-    if (cudaFuncSetAttribute(attn_f32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemLimit) != cudaSuccess)
+    if (!set_smem_limit_once(reinterpret_cast<const void *>(attn_f32_kernel<D>), (int)kSmemLimit))
         return ATTN_ERR_LAUNCH;
     const int nqb = (p.Sq + bq - 1) / bq;
     const int64_t grid = p.bh() * nqb;

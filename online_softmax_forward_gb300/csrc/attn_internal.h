@@ -57,6 +57,24 @@ int noalloc_scratch_ptr(void **ptr);
 // Writes o = 0 and lse = -inf (Skv == 0).
 int launch_empty_keys(void *o, float *lse, const Problem &p, cudaStream_t stream);
 
+// Sets the dynamic shared-memory limit of a kernel on the current device the
+// first time it is asked for that (kernel, device) pair; later calls only
+// look it up.  Returns false if the CUDA call fails.
+bool set_smem_limit_once(const void *func, int bytes);
+// Number of SMs of the current device, cached per device (0 on error).
+int device_sm_count();
+
+// Host-staged calls (attn_fwd_staged) of at least kStagedMinBytes of input
+// run in kStagedChunks chunks of (batch, head) slices on two library streams
+// of the device, so that copies overlap the kernels.
+constexpr int kStagedChunks = 4;
+constexpr size_t kStagedMinBytes = (size_t)4 << 20;
+struct StagedStreams {
+    cudaStream_t st[2];
+    cudaEvent_t start, done[2];
+};
+StagedStreams *staged_streams();  // created once per device; nullptr on failure
+
 // Device status word helpers (attn_api.cu).
 int *status_word_device_ptr();
 

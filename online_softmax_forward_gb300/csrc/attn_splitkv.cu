@@ -428,9 +428,7 @@ int launch_partial(const void *q, const void *k, const void *v, float *po, float
     constexpr size_t smem = skv_smem_bytes<D, T, RB>();
     static_assert(smem <= kSkvSmemLimit, "split-KV shared memory");
     auto kern = splitkv_partial_kernel<D, T, RB>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return ATTN_ERR_LAUNCH;
+    if (!set_smem_limit_once(reinterpret_cast<const void *>(kern), (int)smem)) return ATTN_ERR_LAUNCH;
     const dim3 grid((unsigned)p.bh(), (unsigned)n_eff, (unsigned)((p.Sq + RB - 1) / RB));
     kern<<<grid, SkvCfg<D, T>::kWarps * 32, smem, stream>>>(
         reinterpret_cast<const T *>(q), reinterpret_cast<const T *>(k),
@@ -469,8 +467,7 @@ int occupancy_t() {
     constexpr size_t smem = skv_smem_bytes<D, T, RB>();
     auto kern = splitkv_partial_kernel<D, T, RB>;
     int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess ||
+    if (!set_smem_limit_once(reinterpret_cast<const void *>(kern), (int)smem) ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, SkvCfg<D, T>::kWarps * 32,
                                                       smem) != cudaSuccess)
         return 1;

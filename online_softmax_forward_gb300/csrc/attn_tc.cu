@@ -730,13 +730,6 @@ bool make_map(CUtensorMap *m, const void *base, bool bf16, int d, int S, int64_t
     return r == CUDA_SUCCESS;
 }
 
-int num_sms() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
-
 template <int D, bool kBF16>
 int launch_typed(const void *q, const void *k, const void *v, void *o, float *lse,
                  const Problem &pr, cudaStream_t stream) {
@@ -774,7 +767,7 @@ int launch_typed(const void *q, const void *k, const void *v, void *o, float *ls
     p.out_f32 = (pr.dtype == ATTN_BF16_OUT_F32 || pr.dtype == ATTN_F16_OUT_F32) ? 1 : 0;
     p.hook = test_hook();
     p.timeout_ns = watchdog_ns();
-    const int sms = num_sms();
+    const int sms = device_sm_count();
     if (sms <= 0) return ATTN_ERR_CUDA;
     const int grid = (int)(n_units < sms ? n_units : sms);
     auto kern = attn_tc_kernel<D, kBF16>;
@@ -788,8 +781,7 @@ int launch_typed(const void *q, const void *k, const void *v, void *o, float *ls
         regs_ok = (fa.numRegs == kLaunchRegs && fa.maxThreadsPerBlock >= kThreads) ? 1 : 0;
     }
     if (!regs_ok) return ATTN_ERR_LAUNCH;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess)
+    if (!set_smem_limit_once(reinterpret_cast<const void *>(kern), C::kSmemBytes))
         return ATTN_ERR_LAUNCH;
     kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();

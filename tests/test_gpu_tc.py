@@ -194,3 +194,40 @@ def test_staged_host_buffers_match_device_call():
     o_dev, l_dev = pkg.attention(q.cuda(), k.cuda(), v.cuda(), causal=True)
     torch.cuda.synchronize()
     assert torch.equal(oh, o_dev.cpu()) and torch.equal(lh, l_dev.cpu())
+
+
+@pytest.mark.parametrize("case", [
+    # B, H, Sq, Skv, d, causal, dtype: >= 4 MiB of input, so the call runs in chunks
+    (2, 8, 1024, 1024, 128, True, torch.bfloat16),
+    (1, 5, 700, 1300, 64, True, torch.float16),
+    (2, 3, 600, 600, 64, False, torch.float32),
+])
+def test_staged_chunked_matches_device_call(case):
+    """Large host-staged calls are cut into chunks of (batch, head) slices on
+    two library streams; the result is the same as the device call, and work
+    queued on the caller's stream afterwards sees it complete."""
+    ensure_built()
+    B, H, Sq, Skv, d, causal, dt = case
+    q, k, v = (t.to(dt) for t in qkv_inputs.normal_qkv(B, H, Sq, Skv, d, seed=Sq + H))
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty((B, H, Sq, d), dtype=dt).pin_memory()
+    lh = torch.empty((B, H, Sq), dtype=torch.float32).pin_memory()
+    dq, dk, dv = (torch.empty_like(t, device="cuda") for t in (q, k, v))
+    do_ = torch.empty((B, H, Sq, d), dtype=dt, device="cuda")
+    dl = torch.empty((B, H, Sq), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    code = pkg.dtype_code(dt)
+    st = pkg.attn_fwd_staged(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), oh.data_ptr(),
+                             lh.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                             do_.data_ptr(), dl.data_ptr(), B, H, Sq, Skv, d, int(causal), 0.0,
+                             code, s.cuda_stream)
+    assert st == pkg.ATTN_OK
+    with torch.cuda.stream(s):
+        after = do_.float().sum()  # queued on the caller's stream after the call
+    s.synchronize()
+    assert pkg.attn_check_status(s.cuda_stream) == pkg.ATTN_OK
+    o_dev, l_dev = pkg.attention(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, o_dev.cpu()) and torch.equal(lh, l_dev.cpu())
+    assert torch.equal(do_, o_dev)
+    assert after.item() == o_dev.float().sum().item()
