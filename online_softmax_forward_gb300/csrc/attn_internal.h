@@ -67,7 +67,10 @@ int device_sm_count();
 // Host-staged calls (attn_fwd_staged) of at least kStagedMinBytes of input
 // run in kStagedChunks chunks of (batch, head) slices on two library streams
 // of the device, so that copies overlap the kernels.
-constexpr int kStagedChunks = 4;
+#ifndef ATTN_STAGED_CHUNKS
+#define ATTN_STAGED_CHUNKS 4
+#endif
+constexpr int kStagedChunks = ATTN_STAGED_CHUNKS;
 constexpr size_t kStagedMinBytes = (size_t)4 << 20;
 struct StagedStreams {
     cudaStream_t st[2];
