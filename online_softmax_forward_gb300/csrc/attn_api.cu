@@ -214,8 +214,8 @@ static int fwd_impl(const void *q, const void *k, const void *v, void *o, float 
     if (st != ATTN_OK) return st;
     if (p.Skv == 0) return launch_empty_keys(o, lse, p, stream);
     if (p.dtype == ATTN_F32)
-        return launch_f32((const float *)q, (const float *)k, (const float *)v, (float *)o,
-                          lse, p, 32, 64, stream);
+        return launch_f32_tiled((const float *)q, (const float *)k, (const float *)v, (float *)o,
+                                lse, p, stream);
     return launch_tc(q, k, v, o, lse, p, stream);
 }
 

@@ -5,14 +5,27 @@
 // ("Online normalization"), in fp32, for small and latency-bound shapes and
 // for tile-size invariance tests.  Tile sizes are runtime values.
 //
-// One CTA owns one block of block_q query rows of one (batch, head) slice and
-// walks the key/value blocks of block_kv rows; each block is staged in shared
-// memory once and used by every query row of the CTA.  One warp handles one
-// query row at a time: lanes split the keys of the tile for the scores
-// (q . k, q broadcast from shared memory), warp shuffles give the tile
-// maximum and the sum of exponentials, and lanes split the head dimension for
-// the P.V product.  Per-row state (running max m, normaliser l, accumulator a)
-// lives in shared memory between key tiles.
+// Two kernels compute the same thing:
+//
+// attn_f32_tiled_kernel (attn_fwd): fixed tiles of 32 query rows by 64 keys,
+// 128 threads, register-blocked.  Thread (ty, tx), ty in [0, 8), tx in
+// [0, 16), owns the 4 x 4 scores of rows ty + 8i and keys tx + 16j, so every
+// float4 read from shared memory feeds four FMAs; the row maximum and sum are
+// reduced over the 16 lanes of a half-warp.  It also owns O for rows ty + 8i
+// and columns tx*W + 64c (W = 4 for d >= 64), kept in registers across the
+// whole key loop together with the row state (m, l), so only P goes through
+// shared memory (written and read by the same half-warp).  K/V tiles are
+// double buffered with cp.async.
+//
+// attn_f32_kernel (attn_fwd_f32_blocked): runtime tile sizes, down to 1 x 1,
+// for the tile-size invariance tests.  One CTA owns one block of block_q
+// query rows and walks the key/value blocks of block_kv rows; each block is
+// staged in shared memory once and used by every query row of the CTA.  One
+// warp handles one query row at a time: lanes split the keys of the tile for
+// the scores, warp shuffles give the tile maximum and the sum of
+// exponentials, and lanes split the head dimension for the P.V product.
+// Per-row state (running max m, normaliser l, accumulator a) lives in shared
+// memory between key tiles.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -177,6 +190,323 @@ attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
     }
 }
 
+// ---------------------------------------------------------------- tiled kernel
+constexpr int kTQ = 32;         // query rows per CTA
+constexpr int kTK = 64;         // keys per tile
+constexpr int kWG = 128;        // threads of one warpgroup
+constexpr int kLdP = kTK + 16;  // P row stride: rows 2 apart land 32 banks apart
+
+// KS warpgroups share the query block and take the key tiles in turn
+// (tile j goes to warpgroup j mod KS); each has its own K/V stages and P.
+template <int D, int KS>
+struct TiledCfg {
+    static constexpr int kLd = D + 4;                // Q and K row stride, floats
+    static constexpr int kW = D >= 64 ? 4 : D / 16;  // contiguous O columns per group
+    static constexpr int kNC = D / (16 * kW);        // column groups per thread
+    static constexpr int kStageK = 2 * kTK * kLd;    // floats of one warpgroup's K stages
+    static constexpr int kStageV = 2 * kTK * D;
+    static constexpr int kOffK = kTQ * kLd;
+    static constexpr int kOffV = kOffK + KS * kStageK;
+    static constexpr int kOffP = kOffV + KS * kStageV;
+    static constexpr size_t kSmemBytes = sizeof(float) * (size_t)(kOffP + KS * kTQ * kLdP);
+    // per-thread state a second warpgroup hands over: m, l and O, 4 rows each
+    static constexpr int kStateFloats = 8 + 4 * kNC * kW;
+    static_assert(KS == 1 || kStateFloats * kWG <= kStageK, "state must fit the K stages");
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void *ptr) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+// 16-byte global -> shared copy; src_bytes = 0 writes zeros without reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait1() {
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait0() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+// barrier of the 128 threads of warpgroup g (ids 1.., 0 is __syncthreads)
+__device__ __forceinline__ void wg_sync(int g) {
+    asm volatile("bar.sync %0, %1;" ::"r"(g + 1), "n"(kWG) : "memory");
+}
+
+// rows [row0, row0 + n) of a [S, D] slice into a shared tile of row stride
+// ld by `nthr` threads (this one is `tid`); rows at or past `valid` are
+// zero-filled.
+template <int D>
+__device__ __forceinline__ void stage_async(float *dst, int ld, const float *__restrict__ src,
+                                            int row0, int n, int valid, int tid, int nthr) {
+    constexpr int V4 = D / 4;
+    for (int f = tid; f < n * V4; f += nthr) {
+        const int r = f / V4, c = (f - r * V4) * 4;
+        const bool in = row0 + r < valid;
+        const float *s = in ? src + (size_t)(row0 + r) * D + c : src;
+        cp_async16(smem_addr(dst + r * ld + c), s, in ? 16 : 0);
+    }
+}
+
+template <int D, int KS>
+__global__ void __launch_bounds__(KS * kWG, 1)
+attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
+                      const float *__restrict__ v, float *__restrict__ o,
+                      float *__restrict__ lse, int Sq, int Skv, int causal, float scale_log2,
+                      int nqb) {
+    using C = TiledCfg<D, KS>;
+    constexpr int LD = C::kLd, W = C::kW, NC = C::kNC;
+    extern __shared__ __align__(16) float sm[];
+    const int g = threadIdx.x / kWG;    // warpgroup
+    const int tid = threadIdx.x % kWG;  // thread inside the warpgroup
+    float *Qs = sm;
+    float *Ks = sm + C::kOffK + g * C::kStageK;  // [2][kTK][LD]
+    float *Vs = sm + C::kOffV + g * C::kStageV;  // [2][kTK][D]
+    float *Ps = sm + C::kOffP + g * kTQ * kLdP;  // [kTQ][kLdP]
+
+    const int tx = tid & 15, ty = tid >> 4;
+    const int64_t bh = blockIdx.x / nqb;
+    const int q0 = (blockIdx.x % nqb) * kTQ;
+    const int q_end = min(q0 + kTQ, Sq);
+    const int off = Skv - Sq;  // causal: key j visible to query i iff j <= i + off
+    const float *qg = q + (size_t)bh * Sq * D;
+    const float *kg = k + (size_t)bh * Skv * D;
+    const float *vg = v + (size_t)bh * Skv * D;
+
+    // keys visible to each of this thread's rows: [0, lim[i])
+    int lim[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        lim[i] = causal ? min(Skv, q0 + ty + 8 * i + off + 1) : Skv;
+    const int kv_stop = causal ? min(Skv, q_end + off) : Skv;
+    const int ntiles = kv_stop > 0 ? (kv_stop + kTK - 1) / kTK : 0;
+
+    float m[4], l[4], acc[4][NC][W];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int w = 0; w < W; ++w) acc[i][c][w] = 0.f;
+    }
+
+    // Q (by every thread) and the first tile of each warpgroup, then one
+    // CTA barrier: from here on Q is read-only and each warpgroup syncs alone
+    if (ntiles > 0) {
+        stage_async<D>(Qs, LD, qg, q0, kTQ, Sq, threadIdx.x, KS * kWG);
+        if (g < ntiles) {
+            stage_async<D>(Ks, LD, kg, g * kTK, kTK, Skv, tid, kWG);
+            stage_async<D>(Vs, D, vg, g * kTK, kTK, Skv, tid, kWG);
+        }
+        cp_async_commit();
+        cp_async_wait0();
+    }
+    __syncthreads();
+    for (int jt = g, n = 0; jt < ntiles; jt += KS, ++n) {
+        const int st = n & 1, kv0 = jt * kTK;
+        if (jt + KS < ntiles) {  // the other stage was released at the end of the last tile
+            stage_async<D>(Ks + (st ^ 1) * kTK * LD, LD, kg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+            stage_async<D>(Vs + (st ^ 1) * kTK * D, D, vg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+        }
+        cp_async_commit();
+        cp_async_wait1();  // everything but the copies just issued has landed
+        wg_sync(g);
+        const float *Kt = Ks + st * kTK * LD;
+        const float *Vt = Vs + st * kTK * D;
+
+        // S = Q K^T for rows ty + 8i, keys tx + 16j
+        float s[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < D; c += 4) {
+            float4 qa[4], kb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                qa[i] = *reinterpret_cast<const float4 *>(Qs + (ty + 8 * i) * LD + c);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                kb[j] = *reinterpret_cast<const float4 *>(Kt + (tx + 16 * j) * LD + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float x = s[i][j];
+                    x = fmaf(qa[i].x, kb[j].x, x);
+                    x = fmaf(qa[i].y, kb[j].y, x);
+                    x = fmaf(qa[i].z, kb[j].z, x);
+                    x = fmaf(qa[i].w, kb[j].w, x);
+                    s[i][j] = x;
+                }
+        }
+
+        // online softmax per row, in log2 units: masked keys count as -inf
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool vis = kv0 + tx + 16 * j < lim[i];
+                s[i][j] = vis ? s[i][j] * scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[i][j]);
+            }
+#pragma unroll
+            for (int w = 8; w > 0; w >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, w));
+            const float m_new = fmaxf(m[i], mx);
+            float alpha = 1.f, sum = 0.f;
+            if (m_new == -INFINITY) {  // no visible key yet: P = 0, nothing to rescale
+#pragma unroll
+                for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+            } else {
+                alpha = m[i] == -INFINITY ? 0.f : exp2f(m[i] - m_new);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    s[i][j] = exp2f(s[i][j] - m_new);
+                    sum += s[i][j];
+                }
+            }
+#pragma unroll
+            for (int w = 8; w > 0; w >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
+            m[i] = m_new;
+            l[i] = l[i] * alpha + sum;
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+#pragma unroll
+                for (int w = 0; w < W; ++w) acc[i][c][w] *= alpha;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) Ps[(ty + 8 * i) * kLdP + tx + 16 * j] = s[i][j];
+        }
+        __syncwarp();  // the rows of P this half-warp reads were written by it
+
+        // O += P V for rows ty + 8i, columns tx*W + 64c
+#pragma unroll 2
+        for (int kk = 0; kk < kTK; kk += 4) {
+            float4 pa[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                pa[i] = *reinterpret_cast<const float4 *>(Ps + (ty + 8 * i) * kLdP + kk);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float *vr = Vt + (kk + u) * D + tx * W;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    float vv[W];
+                    if constexpr (W == 4) {
+                        const float4 t4 = *reinterpret_cast<const float4 *>(vr + 64 * c);
+                        vv[0] = t4.x; vv[1] = t4.y; vv[2] = t4.z; vv[3] = t4.w;
+                    } else if constexpr (W == 2) {
+                        const float2 t2 = *reinterpret_cast<const float2 *>(vr + 64 * c);
+                        vv[0] = t2.x; vv[1] = t2.y;
+                    } else {
+                        vv[0] = vr[64 * c];
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float pi = u == 0 ? pa[i].x : u == 1 ? pa[i].y : u == 2 ? pa[i].z : pa[i].w;
+#pragma unroll
+                        for (int w = 0; w < W; ++w) acc[i][c][w] = fmaf(pi, vv[w], acc[i][c][w]);
+                    }
+                }
+            }
+        }
+        wg_sync(g);  // this stage and P are free for the next tile
+    }
+
+    if constexpr (KS == 2) {
+        // warpgroup 1 hands (m, l, O) over through its own K stages, laid out
+        // [field][thread]; warpgroup 0 merges them into its own state the way
+        // two partial softmax states combine: rescale both to the larger max
+        float *xs = sm + C::kOffK + C::kStageK;
+        if (g == 1) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                xs[i * kWG + tid] = m[i];
+                xs[(4 + i) * kWG + tid] = l[i];
+#pragma unroll
+                for (int c = 0; c < NC; ++c)
+#pragma unroll
+                    for (int w = 0; w < W; ++w)
+                        xs[(8 + (i * NC + c) * W + w) * kWG + tid] = acc[i][c][w];
+            }
+        }
+        __syncthreads();
+        if (g == 1) return;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float m1 = xs[i * kWG + tid], l1 = xs[(4 + i) * kWG + tid];
+            const float mm = fmaxf(m[i], m1);
+            const float a0 = m[i] == -INFINITY ? 0.f : exp2f(m[i] - mm);
+            const float a1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mm);
+            m[i] = mm;
+            l[i] = l[i] * a0 + l1 * a1;
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+#pragma unroll
+                for (int w = 0; w < W; ++w)
+                    acc[i][c][w] = acc[i][c][w] * a0 + xs[(8 + (i * NC + c) * W + w) * kWG + tid] * a1;
+        }
+    }
+
+    // O = acc / l and lse = m + log2(l), in natural units; rows that saw no key: 0 and -inf
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int row = q0 + ty + 8 * i;
+        if (row >= Sq) continue;
+        const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
+        float *orow = o + ((size_t)bh * Sq + row) * D + tx * W;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            if constexpr (W == 4) {
+                *reinterpret_cast<float4 *>(orow + 64 * c) =
+                    make_float4(acc[i][c][0] * inv, acc[i][c][1] * inv, acc[i][c][2] * inv,
+                                acc[i][c][3] * inv);
+            } else {
+#pragma unroll
+                for (int w = 0; w < W; ++w) orow[64 * c + w] = acc[i][c][w] * inv;
+            }
+        }
+        if (lse && tx == 0)
+            lse[(size_t)bh * Sq + row] =
+                l[i] > 0.f ? (m[i] + log2f(l[i])) * 0.69314718055994530942f : -INFINITY;
+    }
+}
+
+template <int D, int KS>
+int launch_tiled_ks(const float *q, const float *k, const float *v, float *o, float *lse,
+                    const Problem &p, int64_t grid, int nqb, cudaStream_t stream) {
+    constexpr size_t smem = TiledCfg<D, KS>::kSmemBytes;
+    if (!set_smem_limit_once(reinterpret_cast<const void *>(attn_f32_tiled_kernel<D, KS>),
+                             (int)smem))
+        return ATTN_ERR_LAUNCH;
+    attn_f32_tiled_kernel<D, KS><<<(unsigned)grid, KS * kWG, smem, stream>>>(
+        q, k, v, o, lse, p.Sq, p.Skv, p.causal, p.scale * 1.4426950408889634f, nqb);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+// Fewer query blocks than SMs: two warpgroups per block split its key tiles,
+// so that each SM runs twice the warps (d <= 64, where both fit in shared
+// memory).  Otherwise one warpgroup per block and several blocks per SM.
+template <int D>
+int launch_tiled_d(const float *q, const float *k, const float *v, float *o, float *lse,
+                   const Problem &p, cudaStream_t stream) {
+    const int nqb = (p.Sq + kTQ - 1) / kTQ;
+    const int64_t grid = p.bh() * nqb;
+    if (grid > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+    if constexpr (D <= 64) {
+        const int sms = device_sm_count();
+        if (sms > 0 && grid < sms) return launch_tiled_ks<D, 2>(q, k, v, o, lse, p, grid, nqb, stream);
+    }
+    return launch_tiled_ks<D, 1>(q, k, v, o, lse, p, grid, nqb, stream);
+}
+
 __global__ void fill_empty_kernel(uint8_t *o, size_t o_bytes, float *lse, size_t n_lse) {
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < o_bytes; t += stride)
@@ -214,6 +544,17 @@ int launch_f32(const float *q, const float *k, const float *v, float *o, float *
     case 32: return launch_d<32>(q, k, v, o, lse, p, block_q, block_kv, stream);
     case 64: return launch_d<64>(q, k, v, o, lse, p, block_q, block_kv, stream);
     case 128: return launch_d<128>(q, k, v, o, lse, p, block_q, block_kv, stream);
+    default: return ATTN_ERR_INVALID_ARG;
+    }
+}
+
+int launch_f32_tiled(const float *q, const float *k, const float *v, float *o, float *lse,
+                     const Problem &p, cudaStream_t stream) {
+    switch (p.d) {
+    case 16: return launch_tiled_d<16>(q, k, v, o, lse, p, stream);
+    case 32: return launch_tiled_d<32>(q, k, v, o, lse, p, stream);
+    case 64: return launch_tiled_d<64>(q, k, v, o, lse, p, stream);
+    case 128: return launch_tiled_d<128>(q, k, v, o, lse, p, stream);
     default: return ATTN_ERR_INVALID_ARG;
     }
 }

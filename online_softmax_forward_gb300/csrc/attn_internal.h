@@ -27,6 +27,9 @@ int launch_f32(const float *q, const float *k, const float *v, float *o,
                float *lse, const Problem &p, int block_q, int block_kv,
                cudaStream_t stream);
 bool f32_tiles_fit(int d, int block_q, int block_kv);
+// Register-tiled fp32 kernel with fixed 32 x 64 tiles (the attn_fwd path).
+int launch_f32_tiled(const float *q, const float *k, const float *v, float *o,
+                     float *lse, const Problem &p, cudaStream_t stream);
 
 // 16-bit tensor-core path (attn_tc.cu).
 int launch_tc(const void *q, const void *k, const void *v, void *o, float *lse,

@@ -129,3 +129,21 @@ def test_deterministic_and_lse_optional():
     o3 = pkg.attention(q, k, v, causal=True, return_lse=False)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("bh", [(1, 2), (2, 40)])
+@pytest.mark.parametrize("sq,skv", [(130, 37), (130, 300), (300, 130)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_attn_fwd_tiled_kernel(d, bh, sq, skv, causal):
+    """attn_fwd's register-tiled kernel (32 query rows x 64 keys per tile).
+    With fewer query blocks than SMs (B*H = 2) two warpgroups per block take
+    the key tiles in turn and merge their states (d <= 64); with more
+    (B*H = 80) one warpgroup per block does it all.  Ragged rows and keys,
+    one key tile only (the second warpgroup gets none), an odd number of
+    key tiles, and causal rows with no visible key (Sq > Skv)."""
+    B, H = bh
+    q, k, v = f32(*qkv_inputs.normal_qkv(B, H, sq, skv, d, d + sq + skv + B * H))
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    o, lse = run(q, k, v, causal)
+    assert_f32_parity(o, lse, o_ref, lse_ref)
