@@ -55,6 +55,9 @@ CONFIGS = {
     "b1_h32_s8192_d128_bf16_full": (1, 32, 8192, 8192, 128, False, "bf16", "normal"),
 }
 SPLITKV = {"b4_h32_q1_kv32768_d128_bf16_decode"}
+# fp32 workloads whose arithmetic, not their bytes, bounds them (about 128 FLOP per byte)
+FP32_ALU = {"b2_h4_s512_d64_f32"}
+FP32_FMA_PER_CLK_PER_SM = 128  # CUDA-core FP32 lanes of one SM
 DEFAULT = "b1_h32_s8192_d128_bf16_causal"
 
 
@@ -85,7 +88,12 @@ def load_peaks():
 
 def kernel_source_hash(config_name=DEFAULT):
     """Hash of the source files of the dominant kernel of a workload."""
-    files = ("attn_splitkv.cu",) if config_name in SPLITKV else ("attn_tc.cu", "sm100_ptx.cuh")
+    if config_name in SPLITKV:
+        files = ("attn_splitkv.cu",)
+    elif CONFIGS[config_name][6] == "f32":
+        files = ("attn_f32.cu",)
+    else:
+        files = ("attn_tc.cu", "sm100_ptx.cuh")
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(ROOT, "online_softmax_forward_gb300", "csrc", f), "rb") as fh:
@@ -430,10 +438,21 @@ def main(argv=None):
         # fp16 and bf16 share the dense tensor-core rate: the bf16 measured peak serves both
         peak, unit, bound = peaks["bf16_tflops"], "TFLOP/s", "tensor"
         achieved = tflops
+        peak_source = peaks["source"] + " burst bf16 (kernel timed alone)"
+    elif args.config in FP32_ALU:
+        # FP32 FMA rate from the unit count and the maximum SM clock
+        import torch
+        sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
+        mhz = (r["clocks"] or {}).get("sm_max_mhz") or 2070.0
+        peak = sms * FP32_FMA_PER_CLK_PER_SM * 2 * mhz * 1e6 / 1e12
+        unit, bound, achieved = "TFLOP/s", "alu", tflops
+        peak_source = "derived: %d SMs x %d FP32 FMA/clk x 2 FLOP x %.0f MHz" % (
+            sms, FP32_FMA_PER_CLK_PER_SM, mhz)
     else:
         # decode and the small fp32 cases: compulsory bytes against HBM
         peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
         achieved = compulsory_bytes(cfg) / (r["ms"] * 1e-3) / 1e9
+        peak_source = peaks["source"] + " copy GB/s"
     traffic = profiled_traffic(args.config)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -444,8 +463,7 @@ def main(argv=None):
                                    if dt in ("bf16", "f16") else None),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": peaks["source"] + (" burst bf16 (kernel timed alone)"
-                                                       if bound == "tensor" else " copy GB/s")},
+                     "peak_source": peak_source},
         "e2e": {"value": world * r["flops"] / r["e2e_s"] / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": args.steps * r["launches_per_step"],
