@@ -533,6 +533,13 @@ void splitkv_chunking(int Skv, int n_splits, int *chunk, int *n_eff) {
 // The split count with the smallest estimated time: waves of CTAs over the
 // GPU's resident slots times the key tiles each warp walks, plus a small
 // charge per split for the merge; at least two tiles per warp in a split.
+// Cost of one CTA beyond its key tiles (launch, filling the copy ring, the
+// shared-memory merge of the warps, the partial write), in units of one
+// 32-key tile step per warp.  Fitted to split-count sweeps of a 4 x 32-head,
+// 32768-key decode on GB300, where one CTA costs about 3 us on top of its
+// tiles (about two tile steps).
+constexpr double kCtaFixedTiles = 2.0;
+
 int splitkv_choose(const Problem &p, int sms) {
     const int64_t rows_blocks = (p.Sq + splitkv_row_block(p.Sq) - 1) / splitkv_row_block(p.Sq);
     const int64_t base = p.bh() * rows_blocks;
@@ -550,7 +557,7 @@ int splitkv_choose(const Problem &p, int sms) {
         if (n_eff != n) continue;  // the same chunking as a smaller count
         const int64_t waves = (base * n + slots - 1) / slots;
         const int64_t tiles = ((chunk + kTileKeys - 1) / kTileKeys + W - 1) / W;
-        const double cost = (double)waves * (double)tiles + 0.02 * n;
+        const double cost = (double)waves * ((double)tiles + kCtaFixedTiles) + 0.02 * n;
         if (cost < best_cost) {
             best_cost = cost;
             best = n;

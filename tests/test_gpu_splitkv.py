@@ -135,7 +135,7 @@ def test_plan_fills_the_device():
     st, n, ws = pkg.attn_splitkv_plan(1, 32, 1, 32768, 128, pkg.ATTN_BF16)
     assert st == pkg.ATTN_OK and 1 <= n <= 256
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert 32 * n >= 2 * sms
+    assert 32 * n >= sms  # every SM gets at least one partial block
     st2, ws2 = pkg.attn_splitkv_workspace_size(1, 32, 1, 128, n)
     assert st2 == pkg.ATTN_OK and ws2 == ws
 
