@@ -85,6 +85,12 @@ typedef enum attn_dtype {
  * blocks (the key block of deepnotes "Correctness first"); the 16-bit types
  * run the tensor-core kernel with 128 x 128 tiles.
  * Requires a compute capability 10.3 device (GB300) for every dtype.
+ *
+ * CUDA graphs: the first call on a device sets up per-device state (kernel
+ * attributes, the status word, which is allocated once).  After that a call
+ * only enqueues one kernel on `stream` (two for attn_fwd_splitkv) and may be
+ * captured into a CUDA graph; a replay reads whatever the captured pointers
+ * hold at replay time.  Make the first call before capturing.
  */
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              int B, int H, int Sq, int Skv, int d, int causal, float scale,
