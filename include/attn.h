@@ -87,8 +87,8 @@ typedef enum attn_dtype {
  * Requires a compute capability 10.3 device (GB300) for every dtype.
  *
  * CUDA graphs: the first call on a device sets up per-device state (kernel
- * attributes, the status word, which is allocated once).  After that a call
- * only enqueues one kernel on `stream` (two for attn_fwd_splitkv) and may be
+ * attributes, the address of the status word).  After that a call only
+ * enqueues one kernel on `stream` (two for attn_fwd_splitkv) and may be
  * captured into a CUDA graph; a replay reads whatever the captured pointers
  * hold at replay time.  Make the first call before capturing.
  */
