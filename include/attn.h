@@ -168,9 +168,11 @@ int attn_splitkv_workspace_size(int B, int H, int Sq, int d, int n_splits, size_
 
 /*
  * attn_splitkv_plan -- the split count the library would pick on the current
- * device (enough CTAs to fill every SM several times over, at least two
- * 32-key tiles per warp in each split) and, if workspace_bytes is not NULL,
- * the workspace size for it.  Needs a compute capability 10.3 device.
+ * device and, if workspace_bytes is not NULL, the workspace size for it.
+ * The count minimises an estimate of the time: waves of CTAs over the
+ * device's resident CTA slots times the 32-key tiles each warp walks plus a
+ * fixed cost per CTA (about two tiles), with at least two tiles per warp in
+ * each split.  Needs a compute capability 10.3 device.
  */
 int attn_splitkv_plan(int B, int H, int Sq, int Skv, int d, int dtype, int *n_splits,
                       size_t *workspace_bytes);

@@ -530,15 +530,17 @@ void splitkv_chunking(int Skv, int n_splits, int *chunk, int *n_eff) {
     *n_eff = Skv > 0 ? (Skv + c - 1) / c : 1;
 }
 
-// The split count with the smallest estimated time: waves of CTAs over the
-// GPU's resident slots times the key tiles each warp walks, plus a small
-// charge per split for the merge; at least two tiles per warp in a split.
-// Cost of one CTA beyond its key tiles (launch, filling the copy ring, the
-// shared-memory merge of the warps, the partial write), in units of one
-// 32-key tile step per warp.  Fitted to split-count sweeps of a 4 x 32-head,
-// 32768-key decode on GB300, where one CTA costs about 3 us on top of its
-// tiles (about two tile steps).
+// Cost of one CTA beyond its key tiles, in units of one 32-key tile step per
+// warp.  Fitted to split-count sweeps of a 4 x 32-head, 32768-key decode on
+// GB300, where each CTA costs about 3 us on top of its tiles (about two tile
+// steps): time grows with the split count through the merge kernel and the
+// partial kernel alike.
 constexpr double kCtaFixedTiles = 2.0;
+
+// The split count with the smallest estimated time: waves of CTAs over the
+// GPU's resident slots times (the key tiles each warp walks + the fixed cost
+// per CTA), plus a small charge per split for the merge; at least two tiles
+// per warp in a split.
 
 int splitkv_choose(const Problem &p, int sms) {
     const int64_t rows_blocks = (p.Sq + splitkv_row_block(p.Sq) - 1) / splitkv_row_block(p.Sq);
