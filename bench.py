@@ -96,9 +96,17 @@ def kernel_source_hash(config_name=DEFAULT):
         files = ("attn_tc.cu", "sm100_ptx.cuh")
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "online_softmax_forward_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "online_softmax_forward_gb300", "csrc", f)) as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
+
+
+def code_only(src):
+    """CUDA/C++ source with comments removed and whitespace collapsed, so that
+    an edit of comments alone keeps the kernel's hash."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
 
 
 def profiled_traffic(config_name):

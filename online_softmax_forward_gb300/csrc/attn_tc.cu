@@ -27,7 +27,9 @@
 //    A K/V stage is released when both issuers are done with it.
 //  * Warps 0-3 / 4-7 (softmax warpgroups, one per query tile; one thread per
 //    query row, 224 registers each via setmaxnreg) read S from TMEM in two
-//    halves, apply the causal / tail mask, take the row max, exponentiate with
+//    64-key halves (at d = 128 the second load overlaps the first half's row
+//    max; at d = 64 both are in flight at once), apply the causal / tail
+//    mask, take the row max, exponentiate with
 //    ex2 (scores pre-multiplied by scale*log2 e, paired fp32 arithmetic), sum,
 //    and write P as 16-bit values into a shared-memory tile in the MMA's
 //    128-byte-swizzled layout.  The running max is updated lazily: O and l are

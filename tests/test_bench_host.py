@@ -67,3 +67,11 @@ def test_compulsory_bytes_and_paths():
     # the traffic record is keyed by the source of the workload's dominant kernel
     assert bench.kernel_source_hash(bench.DEFAULT) != \
         bench.kernel_source_hash("b4_h32_q1_kv32768_d128_bf16_decode")
+
+
+def test_kernel_hash_ignores_comments_only():
+    a = "int f(int x) {  // one\n  return x + 1; /* two */ }\n"
+    b = "/* header */\nint f(int x) {\n  return x + 1;\n}  // trailing\n"
+    c = "int f(int x) { return x + 2; }"
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
