@@ -132,9 +132,8 @@ int attn_fwd_f32_blocked(const float *q, const float *k, const float *v,
  * the copies of one chunk overlap the kernel of the other.  Those streams
  * start after the work queued on `stream` and `stream` waits for them, so the
  * call behaves as if everything ran on `stream`; concurrent staged calls on
- * one device share the two streams.  After cudaDeviceReset the library's
- * per-device state (these streams, cached device attributes, the status word
- * address) is stale: do not call the library again in that process.
+ * one device share the two streams.  attn_shutdown releases them; call it
+ * before a cudaDeviceReset that the process survives.
  * Sizes and dtype as attn_fwd; host pointers must not be NULL when their
  * tensor is non-empty.
  */
@@ -260,6 +259,22 @@ int attn_merge(const float *o_parts, const float *lse_parts, int n_parts, int64_
  * reports an error, ATTN_OK otherwise.
  */
 int attn_check_status(void *stream);
+
+/*
+ * attn_shutdown -- releases what the library created on the current device
+ * and forgets what it cached about it.  It destroys the two streams and three
+ * events of attn_fwd_staged, after waiting for those streams to finish.  It
+ * clears the cached capability check, SM count and kernel shared-memory
+ * limits, and the device addresses of the status word and of the no-alloc
+ * scratch.  Work the caller queued on its own streams is not waited for.
+ * The next call on the device sets everything up again.  Call it before
+ * cudaDeviceReset if the process goes on using the library, since a reset
+ * invalidates those handles.  It must not run concurrently with other calls
+ * on the same device.  Returns ATTN_OK, or ATTN_ERR_CUDA if destroying a
+ * handle failed; the state is forgotten either way.  Not on the source
+ * pages: resource management of this library.
+ */
+int attn_shutdown(void);
 
 /* Human-readable text for an attn_status value (static storage). */
 const char *attn_strerror(int status);

@@ -22,7 +22,7 @@ __all__ = [
     "attn_fwd", "attn_validate", "attn_fwd_f32_blocked", "attn_fwd_staged",
     "attn_check_status", "attn_strerror", "attn_abi_version", "attn_test_set_hook",
     "attn_splitkv_workspace_size", "attn_splitkv_plan", "attn_fwd_splitkv", "attn_merge",
-    "attn_fwd_splitkv_noalloc",
+    "attn_fwd_splitkv_noalloc", "attn_shutdown",
     "attention", "attention_f32_blocked", "attention_splitkv", "merge", "dtype_code",
 ]
 
@@ -66,6 +66,7 @@ _SIGS = [
     ("attn_merge", _I, [_P, _P, _I, ctypes.c_int64, _I, _P, _P, _I, _P]),
     ("attn_fwd_splitkv_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                       _P]),
+    ("attn_shutdown", _I, []),
 ]
 
 
@@ -147,6 +148,10 @@ def attn_strerror(status):
 
 def attn_abi_version():
     return load_library().attn_abi_version()
+
+
+def attn_shutdown():
+    return load_library().attn_shutdown()
 
 
 def attn_test_set_hook(hook, timeout_ns=0):

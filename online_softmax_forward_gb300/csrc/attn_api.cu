@@ -132,25 +132,46 @@ int *status_word_device_ptr() {
     return g_status_ptr[dev];
 }
 
+namespace {
+StagedStreams g_staged[kMaxDevices];  // the staged path's streams and events per device
+bool g_staged_made[kMaxDevices];
+
+// Destroys whatever part of a StagedStreams exists (null handles are skipped).
+cudaError_t destroy_staged(StagedStreams &r) {
+    cudaError_t first = cudaSuccess;
+    auto keep = [&](cudaError_t e) { if (first == cudaSuccess) first = e; };
+    for (int j = 0; j < 2; ++j) {
+        if (r.st[j]) {
+            keep(cudaStreamSynchronize(r.st[j]));
+            keep(cudaStreamDestroy(r.st[j]));
+        }
+        if (r.done[j]) keep(cudaEventDestroy(r.done[j]));
+    }
+    if (r.start) keep(cudaEventDestroy(r.start));
+    r = StagedStreams{};
+    return first;
+}
+}  // namespace
+
 StagedStreams *staged_streams() {
-    static StagedStreams res[kMaxDevices];
-    static bool made[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!made[dev]) {
-        StagedStreams r;
-        for (int j = 0; j < 2; ++j) {
-            if (cudaStreamCreateWithFlags(&r.st[j], cudaStreamNonBlocking) != cudaSuccess ||
-                cudaEventCreateWithFlags(&r.done[j], cudaEventDisableTiming) != cudaSuccess)
-                return nullptr;
-        }
-        if (cudaEventCreateWithFlags(&r.start, cudaEventDisableTiming) != cudaSuccess)
+    if (!g_staged_made[dev]) {
+        StagedStreams r{};
+        bool ok = true;
+        for (int j = 0; j < 2 && ok; ++j)
+            ok = cudaStreamCreateWithFlags(&r.st[j], cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&r.done[j], cudaEventDisableTiming) == cudaSuccess;
+        ok = ok && cudaEventCreateWithFlags(&r.start, cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            destroy_staged(r);  // nothing half-made is kept
             return nullptr;
-        res[dev] = r;
-        made[dev] = true;
+        }
+        g_staged[dev] = r;
+        g_staged_made[dev] = true;
     }
-    return &res[dev];
+    return &g_staged[dev];
 }
 
 int test_hook() { return g_hook; }
@@ -226,6 +247,32 @@ using namespace attn;
 extern "C" {
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+int attn_shutdown(void) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_OK;  // nothing is ever kept for it
+    cudaError_t e = cudaSuccess;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_staged_made[dev]) {
+            e = destroy_staged(g_staged[dev]);
+            g_staged_made[dev] = false;
+        }
+        g_status_ptr[dev] = nullptr;
+    }
+    __atomic_store_n(&g_device_ok[dev], 0, __ATOMIC_RELEASE);
+    __atomic_store_n(&g_sms[dev], 0, __ATOMIC_RELEASE);
+    {
+        std::lock_guard<std::mutex> lk(g_smem_mu);
+        int n = 0;
+        for (int i = 0; i < g_smem_n; ++i)
+            if (g_smem_done[i].dev != dev) g_smem_done[n++] = g_smem_done[i];
+        g_smem_n = n;
+    }
+    forget_noalloc_scratch(dev);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
 
 const char *attn_strerror(int status) {
     switch (status) {

@@ -56,6 +56,7 @@ int launch_merge(const float *po, const float *pl, int n_parts, int64_t rows, in
 // device).
 constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
 int noalloc_scratch_ptr(void **ptr);
+void forget_noalloc_scratch(int dev);  // attn_shutdown: look the address up again next time
 
 // Writes o = 0 and lse = -inf (Skv == 0).
 int launch_empty_keys(void *o, float *lse, const Problem &p, cudaStream_t stream);

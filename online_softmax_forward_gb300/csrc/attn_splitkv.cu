@@ -497,15 +497,20 @@ int splitkv_occupancy(const Problem &p) {
 
 int splitkv_row_block(int Sq) { return Sq <= 1 ? 1 : kSplitRowBlock; }
 
+namespace {
+constexpr int kScratchMaxDev = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kScratchMaxDev];
+}  // namespace
+
 // Device address of g_noalloc_scratch on the current device, looked up with
 // cudaGetSymbolAddress the first time a device asks and cached after that.
 int noalloc_scratch_ptr(void **ptr) {
-    constexpr int kMaxDev = 64;
-    static std::mutex mu;
-    static void *addr[kMaxDev];
+    constexpr int kMaxDev = kScratchMaxDev;
+    void **addr = g_scratch_addr;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(mu);
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
     if (!addr[dev]) {
         void *p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
@@ -518,6 +523,12 @@ int noalloc_scratch_ptr(void **ptr) {
     }
     *ptr = addr[dev];
     return ATTN_OK;
+}
+
+void forget_noalloc_scratch(int dev) {
+    if (dev < 0 || dev >= kScratchMaxDev) return;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    g_scratch_addr[dev] = nullptr;
 }
 
 // Keys per split (a multiple of 32) and the number of non-empty splits for a

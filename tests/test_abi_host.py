@@ -172,3 +172,11 @@ def test_merge_rejects_invalid_arguments(lib, kw):
 
 def test_merge_empty_rows_is_noop(lib):
     assert merge_call(rows=0, po=None, pl=None, o=None, lse=None) == pkg.ATTN_OK
+
+
+def test_shutdown_without_a_device_reports_cuda_error(lib):
+    """On a host without a GPU there is no current device to release."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host has a GPU: covered by the GPU tests")
+    assert pkg.attn_shutdown() == pkg.ATTN_ERR_CUDA
