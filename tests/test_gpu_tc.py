@@ -29,6 +29,8 @@ SMALL = [
     (1, 1, 5, 700, 128, False),      # decode-like
     (1, 2, 640, 640, 64, True),      # d = 64
     (2, 1, 333, 129, 64, False),
+    (4, 40, 300, 300, 128, True),    # 320 units: three snake rounds over the SMs
+    (2, 80, 260, 260, 64, False),    # 320 units at d = 64, ragged tail tiles
 ]
 
 
