@@ -14,8 +14,11 @@
 // reduced over the 16 lanes of a half-warp.  It also owns O for rows ty + 8i
 // and columns tx*W + 64c (W = 4 for d >= 64), kept in registers across the
 // whole key loop together with the row state (m, l), so only P goes through
-// shared memory (written and read by the same half-warp).  K/V tiles are
-// double buffered with cp.async.
+// shared memory (written and read by the same half-warp).  K/V tiles go
+// through cp.async, double buffered per warpgroup; on grids with fewer
+// blocks than SMs, 2 or 4 warpgroups per block take the key tiles in turn
+// (single buffered with 4, which then overlap one another) and merge their
+// states at the end.
 //
 // attn_f32_kernel (attn_fwd_f32_blocked): runtime tile sizes, down to 1 x 1,
 // for the tile-size invariance tests.  One CTA owns one block of block_q
@@ -203,8 +206,11 @@ struct TiledCfg {
     static constexpr int kLd = D + 4;                // Q and K row stride, floats
     static constexpr int kW = D >= 64 ? 4 : D / 16;  // contiguous O columns per group
     static constexpr int kNC = D / (16 * kW);        // column groups per thread
-    static constexpr int kStageK = 2 * kTK * kLd;    // floats of one warpgroup's K stages
-    static constexpr int kStageV = 2 * kTK * D;
+    // two stages per warpgroup (the next tile loads during this one), or one
+    // stage when four warpgroups share a block (they overlap each other)
+    static constexpr int kNS = KS >= 4 ? 1 : 2;
+    static constexpr int kStageK = kNS * kTK * kLd;  // floats of one warpgroup's K stages
+    static constexpr int kStageV = kNS * kTK * D;
     static constexpr int kOffK = kTQ * kLd;
     static constexpr int kOffV = kOffK + KS * kStageK;
     static constexpr int kOffP = kOffV + KS * kStageV;
@@ -309,13 +315,17 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
     }
     __syncthreads();
     for (int jt = g, n = 0; jt < ntiles; jt += KS, ++n) {
-        const int st = n & 1, kv0 = jt * kTK;
-        if (jt + KS < ntiles) {  // the other stage was released at the end of the last tile
-            stage_async<D>(Ks + (st ^ 1) * kTK * LD, LD, kg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
-            stage_async<D>(Vs + (st ^ 1) * kTK * D, D, vg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+        const int st = C::kNS == 2 ? (n & 1) : 0, kv0 = jt * kTK;
+        if constexpr (C::kNS == 2) {
+            if (jt + KS < ntiles) {  // the other stage was released at the end of the last tile
+                stage_async<D>(Ks + (st ^ 1) * kTK * LD, LD, kg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+                stage_async<D>(Vs + (st ^ 1) * kTK * D, D, vg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+            }
+            cp_async_commit();
+            cp_async_wait1();  // everything but the copies just issued has landed
+        } else {
+            cp_async_wait0();  // this tile, issued at the end of the last one
         }
-        cp_async_commit();
-        cp_async_wait1();  // everything but the copies just issued has landed
         wg_sync(g);
         const float *Kt = Ks + st * kTK * LD;
         const float *Vt = Vs + st * kTK * D;
@@ -418,14 +428,21 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
             }
         }
         wg_sync(g);  // this stage and P are free for the next tile
+        if constexpr (C::kNS == 1) {
+            if (jt + KS < ntiles) {
+                stage_async<D>(Ks, LD, kg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+                stage_async<D>(Vs, D, vg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+                cp_async_commit();
+            }
+        }
     }
 
-    if constexpr (KS == 2) {
-        // warpgroup 1 hands (m, l, O) over through its own K stages, laid out
-        // [field][thread]; warpgroup 0 merges them into its own state the way
-        // two partial softmax states combine: rescale both to the larger max
-        float *xs = sm + C::kOffK + C::kStageK;
-        if (g == 1) {
+    if constexpr (KS > 1) {
+        // warpgroups 1.. hand (m, l, O) over through their own K stages, laid
+        // out [field][thread]; warpgroup 0 merges them into its own state the
+        // way partial softmax states combine: rescale both to the larger max
+        float *xs = sm + C::kOffK + g * C::kStageK;
+        if (g > 0) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 xs[i * kWG + tid] = m[i];
@@ -438,7 +455,10 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
             }
         }
         __syncthreads();
-        if (g == 1) return;
+        if (g > 0) return;
+#pragma unroll 1
+        for (int h = 1; h < KS; ++h) {
+        xs = sm + C::kOffK + h * C::kStageK;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float m1 = xs[i * kWG + tid], l1 = xs[(4 + i) * kWG + tid];
@@ -452,6 +472,7 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
 #pragma unroll
                 for (int w = 0; w < W; ++w)
                     acc[i][c][w] = acc[i][c][w] * a0 + xs[(8 + (i * NC + c) * W + w) * kWG + tid] * a1;
+        }
         }
     }
 
@@ -491,9 +512,11 @@ int launch_tiled_ks(const float *q, const float *k, const float *v, float *o, fl
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
-// Fewer query blocks than SMs: two warpgroups per block split its key tiles,
-// so that each SM runs twice the warps (d <= 64, where both fit in shared
-// memory).  Otherwise one warpgroup per block and several blocks per SM.
+// Fewer query blocks than SMs: several warpgroups per block split its key
+// tiles, so that each SM runs more warps -- four with one K/V stage each at
+// d = 32 and 64, two with two stages at d = 16 (where a warpgroup's state
+// would not fit one stage for the merge).  Otherwise one warpgroup per block
+// and several blocks per SM.
 template <int D>
 int launch_tiled_d(const float *q, const float *k, const float *v, float *o, float *lse,
                    const Problem &p, cudaStream_t stream) {
@@ -502,7 +525,10 @@ int launch_tiled_d(const float *q, const float *k, const float *v, float *o, flo
     if (grid > INT32_MAX) return ATTN_ERR_INVALID_ARG;
     if constexpr (D <= 64) {
         const int sms = device_sm_count();
-        if (sms > 0 && grid < sms) return launch_tiled_ks<D, 2>(q, k, v, o, lse, p, grid, nqb, stream);
+        if (sms > 0 && grid < sms) {
+            if constexpr (D >= 32) return launch_tiled_ks<D, 4>(q, k, v, o, lse, p, grid, nqb, stream);
+            return launch_tiled_ks<D, 2>(q, k, v, o, lse, p, grid, nqb, stream);
+        }
     }
     return launch_tiled_ks<D, 1>(q, k, v, o, lse, p, grid, nqb, stream);
 }

@@ -137,9 +137,10 @@ def test_deterministic_and_lse_optional():
 @pytest.mark.parametrize("causal", [False, True])
 def test_attn_fwd_tiled_kernel(d, bh, sq, skv, causal):
     """attn_fwd's register-tiled kernel (32 query rows x 64 keys per tile).
-    With fewer query blocks than SMs (B*H = 2) two warpgroups per block take
-    the key tiles in turn and merge their states (d <= 64); with more
-    (B*H = 80) one warpgroup per block does it all.  Ragged rows and keys,
+    With fewer query blocks than SMs (B*H = 2) several warpgroups per block
+    take the key tiles in turn and merge their states (four at d = 32 and 64,
+    two at d = 16); with more (B*H = 80), and at d = 128, one warpgroup per
+    block does it all.  Ragged rows and keys,
     one key tile only (the second warpgroup gets none), an odd number of
     key tiles, and causal rows with no visible key (Sq > Skv)."""
     B, H = bh
