@@ -174,6 +174,9 @@ splitkv_partial_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
     const int bh = blockIdx.x, split = blockIdx.y;
     const int row0 = blockIdx.z * RB;
     const int nrows = min(RB, Sq - row0);
+    // the merge kernel that follows may be scheduled now; it waits for this
+    // grid to complete before it reads anything (griddepcontrol.wait)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int off = Skv - Sq;  // causal: key j visible to query i iff j <= i + off
     const int kb = split * chunk;
     int ke = min(Skv, kb + chunk);
@@ -378,6 +381,9 @@ __global__ void __launch_bounds__(kMergeThreads)
 merge_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_parts,
              int64_t rows, int d, TO *__restrict__ o, float *__restrict__ lse) {
     extern __shared__ float wts[];  // [n_parts]
+    // launched as a programmatic dependent of the partial kernel: its results
+    // are complete and visible after this wait (no-op without a predecessor)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float red[kMergeThreads / 32];
     const int64_t row = blockIdx.x;
     TO *orow = o + row * d;
@@ -417,9 +423,19 @@ int launch_merge_t(const float *po, const float *pl, int n_parts, int64_t rows, 
                    float *lse, cudaStream_t stream) {
     if (rows == 0) return ATTN_OK;
     if (rows > INT32_MAX) return ATTN_ERR_INVALID_ARG;
-    merge_kernel<TO><<<(unsigned)rows, kMergeThreads, (size_t)n_parts * sizeof(float), stream>>>(
-        po, pl, n_parts, rows, d, reinterpret_cast<TO *>(o), lse);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = (size_t)n_parts * sizeof(float);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel<TO>, po, pl, n_parts, rows, d,
+                                             reinterpret_cast<TO *>(o), lse);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 template <int D, typename T, int RB>
