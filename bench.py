@@ -54,7 +54,8 @@ CONFIGS = {
     "b1_h64_s8192_d64_bf16_causal": (1, 64, 8192, 8192, 64, True, "bf16", "normal"),
     "b1_h32_s8192_d128_bf16_full": (1, 32, 8192, 8192, 128, False, "bf16", "normal"),
 }
-SPLITKV = {"b4_h32_q1_kv32768_d128_bf16_decode"}
+# few query rows against many keys: the split-KV path (partial kernel + merge)
+SPLITKV = {"b4_h32_q1_kv32768_d128_bf16_decode", "b1_h1_q8_kv1024_d32_f32"}
 # fp32 workloads whose arithmetic, not their bytes, bounds them (about 128 FLOP per byte)
 FP32_ALU = {"b2_h4_s512_d64_f32"}
 FP32_FMA_PER_CLK_PER_SM = 128  # CUDA-core FP32 lanes of one SM
