@@ -233,7 +233,30 @@ def _shapes(q, k, v):
     for t in (q, k, v):
         if not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous")
+    _device_of(q, k, v)
     return B, H, Sq, k.shape[2], d
+
+
+def _device_of(*tensors):
+    """The one CUDA device all tensors live on; raises otherwise (the kernels
+    are handed raw device pointers)."""
+    dev = None
+    for t in tensors:
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors (got %s)" % t.device)
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("tensors on different devices: %s and %s" % (dev, t.device))
+    return dev
+
+
+def _check_out(t, shape, dtype, dev, name):
+    """A caller-provided output must match exactly what the call writes."""
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous %s tensor of shape %s" % (name, dtype, tuple(shape)))
+    if not t.is_cuda or t.device != dev:
+        raise ValueError("%s must be on %s" % (name, dev))
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, out_dtype=None,
@@ -252,12 +275,16 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out_dty
            ATTN_BF16_OUT_F32: torch.float32, ATTN_F16_OUT_F32: torch.float32}[code]
     if out is None:
         out = torch.empty((B, H, Sq, d), dtype=odt, device=q.device)
+    _check_out(out, (B, H, Sq, d), odt, q.device, "out")
     if return_lse and lse is None:
         lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_out(lse, (B, H, Sq), torch.float32, q.device, "lse")
     sc = 0.0 if scale is None else float(scale)
-    st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                  lse.data_ptr() if lse is not None else None, B, H, Sq, Skv, d, causal,
-                  sc, code, _stream_handle(stream))
+    with torch.cuda.device(q.device):
+        st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                      lse.data_ptr() if lse is not None else None, B, H, Sq, Skv, d, causal,
+                      sc, code, _stream_handle(stream))
     _check(st, "attn_fwd")
     return (out, lse) if return_lse else out
 
@@ -270,9 +297,10 @@ def attention_f32_blocked(q, k, v, block_q: int, block_kv: int, causal: bool = F
     out = torch.empty((B, H, Sq, d), dtype=torch.float32, device=q.device)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
     sc = 0.0 if scale is None else float(scale)
-    st = attn_fwd_f32_blocked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                              lse.data_ptr(), B, H, Sq, Skv, d, causal, sc, block_q, block_kv,
-                              _stream_handle(stream))
+    with torch.cuda.device(q.device):
+        st = attn_fwd_f32_blocked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr(), B, H, Sq, Skv, d, causal, sc, block_q,
+                                  block_kv, _stream_handle(stream))
     _check(st, "attn_fwd_f32_blocked")
     return out, lse
 
@@ -293,20 +321,25 @@ def attention_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("q, k, v must share a dtype")
     if n_splits is None:
-        st, n_splits, _ = attn_splitkv_plan(B, H, Sq, Skv, d, code)
+        with torch.cuda.device(q.device):
+            st, n_splits, _ = attn_splitkv_plan(B, H, Sq, Skv, d, code)
         _check(st, "attn_splitkv_plan")
     st, need = attn_splitkv_workspace_size(B, H, Sq, d, n_splits)
     _check(st, "attn_splitkv_workspace_size")
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if not workspace.is_contiguous() or _device_of(workspace) != q.device:
+        raise ValueError("workspace must be a contiguous tensor on %s" % q.device)
     odt = {ATTN_F32: torch.float32, ATTN_BF16: torch.bfloat16, ATTN_F16: torch.float16,
            ATTN_BF16_OUT_F32: torch.float32, ATTN_F16_OUT_F32: torch.float32}[code]
     out = torch.empty((B, H, Sq, d), dtype=odt, device=q.device)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
     sc = 0.0 if scale is None else float(scale)
-    st = attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                          lse.data_ptr(), B, H, Sq, Skv, d, causal, sc, code, n_splits,
-                          workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    with torch.cuda.device(q.device):
+        st = attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr(), B, H, Sq, Skv, d, causal, sc, code, n_splits,
+                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              _stream_handle(stream))
     _check(st, "attn_fwd_splitkv")
     return out, lse
 
@@ -320,12 +353,14 @@ def merge(o_parts, lse_parts, out_dtype=None, stream=None):
     if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
         raise ValueError("partial results are fp32")
     o_parts, lse_parts = o_parts.contiguous(), lse_parts.contiguous()
+    _device_of(o_parts, lse_parts)
     n, rows, d = o_parts.shape
     odt = torch.float32 if out_dtype is None else out_dtype
     code = {torch.float32: ATTN_F32, torch.bfloat16: ATTN_BF16, torch.float16: ATTN_F16}[odt]
     out = torch.empty((rows, d), dtype=odt, device=o_parts.device)
     lse = torch.empty((rows,), dtype=torch.float32, device=o_parts.device)
-    st = attn_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n, rows, d, out.data_ptr(),
-                    lse.data_ptr(), code, _stream_handle(stream))
+    with torch.cuda.device(o_parts.device):
+        st = attn_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n, rows, d, out.data_ptr(),
+                        lse.data_ptr(), code, _stream_handle(stream))
     _check(st, "attn_merge")
     return out, lse

@@ -347,7 +347,8 @@ int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
             cudaStreamWaitEvent(res->st[1], res->start, 0) != cudaSuccess)
             return ATTN_ERR_LAUNCH;
     }
-    for (int i = 0; i < nchunks; ++i) {
+    int err = ATTN_OK;
+    for (int i = 0; i < nchunks && err == ATTN_OK; ++i) {
         // (batch, head) slices [b0, b1) on alternating streams: the copies of
         // one chunk overlap the kernel and the copies of the other
         const int64_t b0 = BH * i / nchunks, b1 = BH * (i + 1) / nchunks;
@@ -358,37 +359,41 @@ int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
         char *doc = (char *)do_ + oq * eout;
         float *dlc = dlse ? dlse + (size_t)b0 * Sq : nullptr;
         if (cudaMemcpyAsync(dqc, (const char *)q_host + oq * ein, cq * ein, cudaMemcpyHostToDevice,
-                            cs) != cudaSuccess)
-            return ATTN_ERR_LAUNCH;
-        if (ckv > 0) {
-            if (cudaMemcpyAsync(dkc, (const char *)k_host + okv * ein, ckv * ein,
-                                cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-                cudaMemcpyAsync(dvc, (const char *)v_host + okv * ein, ckv * ein,
-                                cudaMemcpyHostToDevice, cs) != cudaSuccess)
-                return ATTN_ERR_LAUNCH;
+                            cs) != cudaSuccess) {
+            err = ATTN_ERR_LAUNCH;
+            break;
+        }
+        if (ckv > 0 &&
+            (cudaMemcpyAsync(dkc, (const char *)k_host + okv * ein, ckv * ein,
+                             cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+             cudaMemcpyAsync(dvc, (const char *)v_host + okv * ein, ckv * ein,
+                             cudaMemcpyHostToDevice, cs) != cudaSuccess)) {
+            err = ATTN_ERR_LAUNCH;
+            break;
         }
         Problem sub = p;
         sub.B = 1;
         sub.H = (int)(b1 - b0);
-        st = fwd_impl(dqc, dkc, dvc, doc, dlc, sub, cs);
-        if (st != ATTN_OK) return st;
+        err = fwd_impl(dqc, dkc, dvc, doc, dlc, sub, cs);
+        if (err != ATTN_OK) break;
         if (cudaMemcpyAsync((char *)o_host + oq * eout, doc, cq * eout, cudaMemcpyDeviceToHost,
-                            cs) != cudaSuccess)
-            return ATTN_ERR_LAUNCH;
-        if (lse_host && dlse) {
-            if (cudaMemcpyAsync(lse_host + (size_t)b0 * Sq, dlc, (size_t)(b1 - b0) * Sq * 4,
-                                cudaMemcpyDeviceToHost, cs) != cudaSuccess)
-                return ATTN_ERR_LAUNCH;
-        }
+                            cs) != cudaSuccess ||
+            (lse_host && dlse &&
+             cudaMemcpyAsync(lse_host + (size_t)b0 * Sq, dlc, (size_t)(b1 - b0) * Sq * 4,
+                             cudaMemcpyDeviceToHost, cs) != cudaSuccess))
+            err = ATTN_ERR_LAUNCH;
     }
     if (nchunks > 1) {
-        // the caller's stream continues once both chunk streams are done
+        // the caller's stream continues once both chunk streams are done --
+        // also after a failure, so that work already queued on the library's
+        // streams is ordered before whatever the caller does next
         for (int j = 0; j < 2; ++j)
             if (cudaEventRecord(res->done[j], res->st[j]) != cudaSuccess ||
-                cudaStreamWaitEvent(s, res->done[j], 0) != cudaSuccess)
-                return ATTN_ERR_LAUNCH;
+                cudaStreamWaitEvent(s, res->done[j], 0) != cudaSuccess) {
+                if (err == ATTN_OK) err = ATTN_ERR_LAUNCH;
+            }
     }
-    return ATTN_OK;
+    return err;
 }
 
 int attn_splitkv_workspace_size(int B, int H, int Sq, int d, int n_splits, size_t *bytes) {

@@ -47,6 +47,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <math.h>
 #include <mutex>
 #include <stdint.h>
@@ -789,13 +790,15 @@ int launch_typed(const void *q, const void *k, const void *v, void *o, float *ls
     // The register split inside the kernel (setmaxnreg) needs exactly the pool
     // it was sized for; a build with another entry register count would block
     // in setmaxnreg.inc, so it is refused here instead of launched.
-    static int regs_ok = -1;
-    if (regs_ok < 0) {
+    static std::atomic<int> regs_ok{-1};  // a property of the binary: the same on every device
+    int ok = regs_ok.load(std::memory_order_relaxed);
+    if (ok < 0) {
         cudaFuncAttributes fa;
         if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return ATTN_ERR_UNSUPPORTED_DEVICE;
-        regs_ok = (fa.numRegs == kLaunchRegs && fa.maxThreadsPerBlock >= kThreads) ? 1 : 0;
+        ok = (fa.numRegs == kLaunchRegs && fa.maxThreadsPerBlock >= kThreads) ? 1 : 0;
+        regs_ok.store(ok, std::memory_order_relaxed);
     }
-    if (!regs_ok) return ATTN_ERR_LAUNCH;
+    if (!ok) return ATTN_ERR_LAUNCH;
     if (!set_smem_limit_once(reinterpret_cast<const void *>(kern), C::kSmemBytes))
         return ATTN_ERR_LAUNCH;
     kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);

@@ -180,3 +180,16 @@ def test_shutdown_without_a_device_reports_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("host has a GPU: covered by the GPU tests")
     assert pkg.attn_shutdown() == pkg.ATTN_ERR_CUDA
+
+
+def test_torch_wrappers_reject_host_tensors_before_any_call(lib):
+    """The wrappers hand raw pointers to the kernels: CPU tensors are refused
+    on the host, before anything is launched."""
+    import torch
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        pkg.attention(q, q, q)
+    with pytest.raises(ValueError, match="CUDA"):
+        pkg.attention_splitkv(q, q, q, n_splits=1)
+    with pytest.raises(ValueError, match="CUDA"):
+        pkg.merge(torch.zeros(2, 4, 64), torch.zeros(2, 4))
