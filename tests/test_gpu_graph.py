@@ -55,3 +55,25 @@ def test_graph_replay_matches_direct_call(case):
         torch.cuda.synchronize()
         assert torch.equal(go, o) and torch.equal(gl, lse)
     assert pkg.attn_check_status(None) == pkg.ATTN_OK
+
+
+def test_wrappers_refuse_mismatched_outputs_before_launching():
+    """Caller-provided outputs and workspaces are checked against what the
+    call writes (shape, dtype, contiguity, device) on the host: a mismatch is
+    a ValueError and the output stays untouched."""
+    ensure_built()
+    q, k, v = (t.to(torch.bfloat16).cuda() for t in qkv_inputs.normal_qkv(1, 2, 64, 64, 64, seed=5))
+    bad_shape = torch.full((1, 2, 63, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    bad_dtype = torch.full((1, 2, 64, 64), 7.0, dtype=torch.float16, device="cuda")
+    strided = torch.full((1, 2, 64, 128), 7.0, dtype=torch.bfloat16, device="cuda")[..., ::2]
+    host = torch.full((1, 2, 64, 64), 7.0, dtype=torch.bfloat16)
+    for out in (bad_shape, bad_dtype, strided, host):
+        with pytest.raises(ValueError):
+            pkg.attention(q, k, v, out=out)
+        assert torch.all(out == 7.0)
+    with pytest.raises(ValueError):
+        pkg.attention(q, k, v, lse=torch.zeros((1, 2, 64), dtype=torch.float16, device="cuda"))
+    with pytest.raises(ValueError):
+        pkg.attention_splitkv(q, k, v, n_splits=2, workspace=torch.zeros(1 << 20, dtype=torch.uint8))
+    torch.cuda.synchronize()
+    assert pkg.attn_check_status(None) == pkg.ATTN_OK
