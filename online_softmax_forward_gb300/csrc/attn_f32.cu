@@ -10,15 +10,17 @@
 // attn_f32_tiled_kernel (attn_fwd): fixed tiles of 32 query rows by 64 keys,
 // 128 threads, register-blocked.  Thread (ty, tx), ty in [0, 8), tx in
 // [0, 16), owns the 4 x 4 scores of rows ty + 8i and keys tx + 16j, so every
-// float4 read from shared memory feeds four FMAs; the row maximum and sum are
-// reduced over the 16 lanes of a half-warp.  It also owns O for rows ty + 8i
-// and columns tx*W + 64c (W = 4 for d >= 64), kept in registers across the
-// whole key loop together with the row state (m, l), so only P goes through
-// shared memory (written and read by the same half-warp).  K/V tiles go
-// through cp.async, double buffered per warpgroup; on grids with fewer
-// blocks than SMs, 2 or 4 warpgroups per block take the key tiles in turn
-// (single buffered with 4, which then overlap one another) and merge their
-// states at the end.
+// float4 read from shared memory feeds four FMAs; the row maximum is reduced
+// over the 16 lanes of a half-warp every tile, the row sum once at the end.
+// It also owns O for rows ty + 8i and columns tx*W + 64c (W = 4 for d >= 64),
+// kept in registers across the whole key loop together with the row state
+// (m, l), so only P goes through shared memory (written and read by the same
+// half-warp).  Only tiles that some row of the block cannot see whole are
+// masked.  K/V tiles go through cp.async, in two stages per warpgroup or in
+// one, where the next K loads while this tile's softmax and P V run and the
+// next V while the next scores are taken.  On grids with fewer blocks than
+// SMs, 2 or 4 warpgroups per block take the key tiles in turn and merge their
+// states at the end, each warpgroup finishing a quarter (or half) of the rows.
 //
 // attn_f32_kernel (attn_fwd_f32_blocked): runtime tile sizes, down to 1 x 1,
 // for the tile-size invariance tests.  One CTA owns one block of block_q
@@ -32,6 +34,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <atomic>
 
 #include "attn_internal.h"
 
@@ -200,15 +204,16 @@ constexpr int kWG = 128;        // threads of one warpgroup
 constexpr int kLdP = kTK + 16;  // P row stride: rows 2 apart land 32 banks apart
 
 // KS warpgroups share the query block and take the key tiles in turn
-// (tile j goes to warpgroup j mod KS); each has its own K/V stages and P.
-template <int D, int KS>
+// (tile j goes to warpgroup j mod KS); each has its own P and NS stages of
+// K and V.  With two stages the next tile loads whole during this one; with
+// one, the next K loads once this tile's scores are taken and the next V once
+// its P V is done.
+template <int D, int KS, int NS>
 struct TiledCfg {
     static constexpr int kLd = D + 4;                // Q and K row stride, floats
     static constexpr int kW = D >= 64 ? 4 : D / 16;  // contiguous O columns per group
     static constexpr int kNC = D / (16 * kW);        // column groups per thread
-    // two stages per warpgroup (the next tile loads during this one), or one
-    // stage when four warpgroups share a block (they overlap each other)
-    static constexpr int kNS = KS >= 4 ? 1 : 2;
+    static constexpr int kNS = NS;
     static constexpr int kStageK = kNS * kTK * kLd;  // floats of one warpgroup's K stages
     static constexpr int kStageV = kNS * kTK * D;
     static constexpr int kOffK = kTQ * kLd;
@@ -218,6 +223,7 @@ struct TiledCfg {
     // per-thread state a second warpgroup hands over: m, l and O, 4 rows each
     static constexpr int kStateFloats = 8 + 4 * kNC * kW;
     static_assert(KS == 1 || kStateFloats * kWG <= kStageK, "state must fit the K stages");
+    static_assert(NS == 1 || NS == 2, "one or two stages");
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *ptr) {
@@ -258,20 +264,26 @@ __device__ __forceinline__ void stage_async(float *dst, int ld, const float *__r
     }
 }
 
-template <int D, int KS>
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+template <int D, int KS, int NS>
 __global__ void __launch_bounds__(KS * kWG, 1)
 attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
                       const float *__restrict__ v, float *__restrict__ o,
                       float *__restrict__ lse, int Sq, int Skv, int causal, float scale_log2,
                       int nqb) {
-    using C = TiledCfg<D, KS>;
+    using C = TiledCfg<D, KS, NS>;
     constexpr int LD = C::kLd, W = C::kW, NC = C::kNC;
     extern __shared__ __align__(16) float sm[];
     const int g = threadIdx.x / kWG;    // warpgroup
     const int tid = threadIdx.x % kWG;  // thread inside the warpgroup
     float *Qs = sm;
-    float *Ks = sm + C::kOffK + g * C::kStageK;  // [2][kTK][LD]
-    float *Vs = sm + C::kOffV + g * C::kStageV;  // [2][kTK][D]
+    float *Ks = sm + C::kOffK + g * C::kStageK;  // [kNS][kTK][LD]
+    float *Vs = sm + C::kOffV + g * C::kStageV;  // [kNS][kTK][D]
     float *Ps = sm + C::kOffP + g * kTQ * kLdP;  // [kTQ][kLdP]
 
     const int tx = tid & 15, ty = tid >> 4;
@@ -290,7 +302,12 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
         lim[i] = causal ? min(Skv, q0 + ty + 8 * i + off + 1) : Skv;
     const int kv_stop = causal ? min(Skv, q_end + off) : Skv;
     const int ntiles = kv_stop > 0 ? (kv_stop + kTK - 1) / kTK : 0;
+    // keys below kv_all are visible to every row of the block: tiles that end
+    // there need no mask
+    const int kv_all = causal ? min(Skv, q0 + off + 1) : Skv;
 
+    // m in log2 units; l is this thread's share of the row sum (its own keys),
+    // summed over the half-warp once at the end
     float m[4], l[4], acc[4][NC][W];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -302,35 +319,36 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
             for (int w = 0; w < W; ++w) acc[i][c][w] = 0.f;
     }
 
-    // Q (by every thread) and the first tile of each warpgroup, then one
-    // CTA barrier: from here on Q is read-only and each warpgroup syncs alone
+    // Q and the first K of each warpgroup, then its first V as a second
+    // group, so the first S starts while V is still arriving; one CTA barrier:
+    // from here on Q is read-only and each warpgroup syncs alone
     if (ntiles > 0) {
         stage_async<D>(Qs, LD, qg, q0, kTQ, Sq, threadIdx.x, KS * kWG);
-        if (g < ntiles) {
-            stage_async<D>(Ks, LD, kg, g * kTK, kTK, Skv, tid, kWG);
-            stage_async<D>(Vs, D, vg, g * kTK, kTK, Skv, tid, kWG);
-        }
+        if (g < ntiles) stage_async<D>(Ks, LD, kg, g * kTK, kTK, Skv, tid, kWG);
         cp_async_commit();
-        cp_async_wait0();
+        if (g < ntiles) stage_async<D>(Vs, D, vg, g * kTK, kTK, Skv, tid, kWG);
+        cp_async_commit();
+        cp_async_wait1();
     }
     __syncthreads();
     for (int jt = g, n = 0; jt < ntiles; jt += KS, ++n) {
         const int st = C::kNS == 2 ? (n & 1) : 0, kv0 = jt * kTK;
+        const bool more = jt + KS < ntiles;
         if constexpr (C::kNS == 2) {
-            if (jt + KS < ntiles) {  // the other stage was released at the end of the last tile
+            if (more) {  // the other stage was released at the end of the last tile
                 stage_async<D>(Ks + (st ^ 1) * kTK * LD, LD, kg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
                 stage_async<D>(Vs + (st ^ 1) * kTK * D, D, vg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
             }
             cp_async_commit();
             cp_async_wait1();  // everything but the copies just issued has landed
-        } else {
-            cp_async_wait0();  // this tile, issued at the end of the last one
+            wg_sync(g);
         }
-        wg_sync(g);
+        // one stage: K of this tile has landed and is visible (prologue or
+        // the end of the last tile); V may still be arriving
         const float *Kt = Ks + st * kTK * LD;
         const float *Vt = Vs + st * kTK * D;
 
-        // S = Q K^T for rows ty + 8i, keys tx + 16j
+        // raw scores Q K^T for rows ty + 8i, keys tx + 16j
         float s[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -357,20 +375,35 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
                     s[i][j] = x;
                 }
         }
+        if constexpr (C::kNS == 1) {
+            cp_async_wait0();  // V of this tile, the only copy in flight
+            wg_sync(g);        // K is free for the next tile and V is visible
+            if (more) {
+                stage_async<D>(Ks, LD, kg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+                cp_async_commit();
+            }
+        }
 
-        // online softmax per row, in log2 units: masked keys count as -inf
+        // online softmax per row: the maximum of the raw scores (the scale is
+        // positive, so it commutes with the maximum), then one FMA scales and
+        // shifts each score into log2 units before exp2; masked keys are -inf
+        if (kv0 + kTK > kv_all) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (kv0 + tx + 16 * j >= lim[i]) s[i][j] = -INFINITY;
+        }
+        float mx[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx[i] = fmaxf(fmax3(s[i][0], s[i][1], s[i][2]), s[i][3]);
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], w));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const bool vis = kv0 + tx + 16 * j < lim[i];
-                s[i][j] = vis ? s[i][j] * scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[i][j]);
-            }
-#pragma unroll
-            for (int w = 8; w > 0; w >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, w));
-            const float m_new = fmaxf(m[i], mx);
+            const float m_new = fmaxf(m[i], mx[i] * scale_log2);
             float alpha = 1.f, sum = 0.f;
             if (m_new == -INFINITY) {  // no visible key yet: P = 0, nothing to rescale
 #pragma unroll
@@ -379,12 +412,10 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
                 alpha = m[i] == -INFINITY ? 0.f : exp2f(m[i] - m_new);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    s[i][j] = exp2f(s[i][j] - m_new);
+                    s[i][j] = exp2f(fmaf(s[i][j], scale_log2, -m_new));
                     sum += s[i][j];
                 }
             }
-#pragma unroll
-            for (int w = 8; w > 0; w >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
             m[i] = m_new;
             l[i] = l[i] * alpha + sum;
 #pragma unroll
@@ -429,20 +460,26 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
         }
         wg_sync(g);  // this stage and P are free for the next tile
         if constexpr (C::kNS == 1) {
-            if (jt + KS < ntiles) {
-                stage_async<D>(Ks, LD, kg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+            if (more) {
                 stage_async<D>(Vs, D, vg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
                 cp_async_commit();
+                cp_async_wait1();  // the next K; the next V may still be arriving
+                wg_sync(g);
             }
         }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1) l[i] += __shfl_xor_sync(0xffffffffu, l[i], w);
 
     if constexpr (KS > 1) {
-        // warpgroups 1.. hand (m, l, O) over through their own K stages, laid
-        // out [field][thread]; warpgroup 0 merges them into its own state the
-        // way partial softmax states combine: rescale both to the larger max
-        float *xs = sm + C::kOffK + g * C::kStageK;
-        if (g > 0) {
+        // every warpgroup leaves (m, l, O) in its own K stages, laid out
+        // [field][thread]; warpgroup g then finishes rows i = g, g + KS, ...
+        // of every thread position, combining the KS partial states the way
+        // partial softmax states combine: rescale each to the largest max
+        {
+            float *xs = sm + C::kOffK + g * C::kStageK;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 xs[i * kWG + tid] = m[i];
@@ -455,27 +492,47 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
             }
         }
         __syncthreads();
-        if (g > 0) return;
 #pragma unroll 1
-        for (int h = 1; h < KS; ++h) {
-        xs = sm + C::kOffK + h * C::kStageK;
+        for (int i = g; i < 4; i += KS) {
+            const int row = q0 + ty + 8 * i;
+            if (row >= Sq) continue;
+            float mm = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float m1 = xs[i * kWG + tid], l1 = xs[(4 + i) * kWG + tid];
-            const float mm = fmaxf(m[i], m1);
-            const float a0 = m[i] == -INFINITY ? 0.f : exp2f(m[i] - mm);
-            const float a1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mm);
-            m[i] = mm;
-            l[i] = l[i] * a0 + l1 * a1;
+            for (int h = 0; h < KS; ++h) mm = fmaxf(mm, sm[C::kOffK + h * C::kStageK + i * kWG + tid]);
+            float ll = 0.f, a[NC][W];
 #pragma unroll
             for (int c = 0; c < NC; ++c)
 #pragma unroll
-                for (int w = 0; w < W; ++w)
-                    acc[i][c][w] = acc[i][c][w] * a0 + xs[(8 + (i * NC + c) * W + w) * kWG + tid] * a1;
+                for (int w = 0; w < W; ++w) a[c][w] = 0.f;
+#pragma unroll
+            for (int h = 0; h < KS; ++h) {
+                const float *xs = sm + C::kOffK + h * C::kStageK;
+                const float mh = xs[i * kWG + tid];
+                const float sc = mh == -INFINITY ? 0.f : exp2f(mh - mm);
+                ll = fmaf(xs[(4 + i) * kWG + tid], sc, ll);
+#pragma unroll
+                for (int c = 0; c < NC; ++c)
+#pragma unroll
+                    for (int w = 0; w < W; ++w)
+                        a[c][w] = fmaf(xs[(8 + (i * NC + c) * W + w) * kWG + tid], sc, a[c][w]);
+            }
+            const float inv = ll > 0.f ? 1.f / ll : 0.f;
+            float *orow = o + ((size_t)bh * Sq + row) * D + tx * W;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                if constexpr (W == 4) {
+                    *reinterpret_cast<float4 *>(orow + 64 * c) =
+                        make_float4(a[c][0] * inv, a[c][1] * inv, a[c][2] * inv, a[c][3] * inv);
+                } else {
+#pragma unroll
+                    for (int w = 0; w < W; ++w) orow[64 * c + w] = a[c][w] * inv;
+                }
+            }
+            if (lse && tx == 0)
+                lse[(size_t)bh * Sq + row] =
+                    ll > 0.f ? (mm + log2f(ll)) * 0.69314718055994530942f : -INFINITY;
         }
-        }
-    }
-
+    } else {
     // O = acc / l and lse = m + log2(l), in natural units; rows that saw no key: 0 and -inf
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -498,39 +555,67 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
             lse[(size_t)bh * Sq + row] =
                 l[i] > 0.f ? (m[i] + log2f(l[i])) * 0.69314718055994530942f : -INFINITY;
     }
+    }
 }
 
-template <int D, int KS>
+template <int D, int KS, int NS>
 int launch_tiled_ks(const float *q, const float *k, const float *v, float *o, float *lse,
                     const Problem &p, int64_t grid, int nqb, cudaStream_t stream) {
-    constexpr size_t smem = TiledCfg<D, KS>::kSmemBytes;
-    if (!set_smem_limit_once(reinterpret_cast<const void *>(attn_f32_tiled_kernel<D, KS>),
+    constexpr size_t smem = TiledCfg<D, KS, NS>::kSmemBytes;
+    if (!set_smem_limit_once(reinterpret_cast<const void *>(attn_f32_tiled_kernel<D, KS, NS>),
                              (int)smem))
         return ATTN_ERR_LAUNCH;
-    attn_f32_tiled_kernel<D, KS><<<(unsigned)grid, KS * kWG, smem, stream>>>(
+    attn_f32_tiled_kernel<D, KS, NS><<<(unsigned)grid, KS * kWG, smem, stream>>>(
         q, k, v, o, lse, p.Sq, p.Skv, p.causal, p.scale * 1.4426950408889634f, nqb);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+// Blocks of one warpgroup with two stages that one SM holds at once (shared
+// memory bounds it: one at d = 128, two at d = 64), 0 while unknown.  A
+// property of the kernel and the architecture, so it is asked once.
+template <int D>
+int two_stage_blocks_per_sm() {
+    static std::atomic<int> cached{0};
+    int n = cached.load(std::memory_order_acquire);
+    if (n > 0) return n;
+    constexpr size_t smem = TiledCfg<D, 1, 2>::kSmemBytes;
+    if (!set_smem_limit_once(reinterpret_cast<const void *>(attn_f32_tiled_kernel<D, 1, 2>),
+                             (int)smem))
+        return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_f32_tiled_kernel<D, 1, 2>, kWG,
+                                                      smem) != cudaSuccess) {
+        (void)cudaGetLastError();  // a failed query is not a launch error
+        return 0;
+    }
+    cached.store(n, std::memory_order_release);
+    return n;
 }
 
 // Fewer query blocks than SMs: several warpgroups per block split its key
 // tiles, so that each SM runs more warps -- four with one K/V stage each at
 // d = 32 and 64, two with two stages at d = 16 (where a warpgroup's state
-// would not fit one stage for the merge).  Otherwise one warpgroup per block
-// and several blocks per SM.
+// would not fit one stage for the merge).  Otherwise one warpgroup per block:
+// with two stages while the whole grid is resident at once, and with one
+// stage beyond that, which halves the block's K/V memory so that twice as
+// many blocks share an SM and hide one another's copies (+20 % at
+// B=2, H=40, S=1024, d=64 and at B=2, H=16, S=2048, d=128).
 template <int D>
 int launch_tiled_d(const float *q, const float *k, const float *v, float *o, float *lse,
                    const Problem &p, cudaStream_t stream) {
     const int nqb = (p.Sq + kTQ - 1) / kTQ;
     const int64_t grid = p.bh() * nqb;
     if (grid > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+    const int sms = device_sm_count();
     if constexpr (D <= 64) {
-        const int sms = device_sm_count();
         if (sms > 0 && grid < sms) {
-            if constexpr (D >= 32) return launch_tiled_ks<D, 4>(q, k, v, o, lse, p, grid, nqb, stream);
-            return launch_tiled_ks<D, 2>(q, k, v, o, lse, p, grid, nqb, stream);
+            if constexpr (D >= 32) return launch_tiled_ks<D, 4, 1>(q, k, v, o, lse, p, grid, nqb, stream);
+            return launch_tiled_ks<D, 2, 2>(q, k, v, o, lse, p, grid, nqb, stream);
         }
     }
-    return launch_tiled_ks<D, 1>(q, k, v, o, lse, p, grid, nqb, stream);
+    const int per_sm = two_stage_blocks_per_sm<D>();
+    if (sms > 0 && per_sm > 0 && grid <= (int64_t)sms * per_sm)
+        return launch_tiled_ks<D, 1, 2>(q, k, v, o, lse, p, grid, nqb, stream);
+    return launch_tiled_ks<D, 1, 1>(q, k, v, o, lse, p, grid, nqb, stream);
 }
 
 __global__ void fill_empty_kernel(uint8_t *o, size_t o_bytes, float *lse, size_t n_lse) {

@@ -132,17 +132,21 @@ def test_deterministic_and_lse_optional():
 
 
 @pytest.mark.parametrize("d", [16, 32, 64, 128])
-@pytest.mark.parametrize("bh", [(1, 2), (2, 40)])
+@pytest.mark.parametrize("bh", [(1, 2), (1, 40), (2, 40)])
 @pytest.mark.parametrize("sq,skv", [(130, 37), (130, 300), (300, 130)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_attn_fwd_tiled_kernel(d, bh, sq, skv, causal):
     """attn_fwd's register-tiled kernel (32 query rows x 64 keys per tile).
     With fewer query blocks than SMs (B*H = 2) several warpgroups per block
-    take the key tiles in turn and merge their states (four at d = 32 and 64,
-    two at d = 16); with more (B*H = 80), and at d = 128, one warpgroup per
-    block does it all.  Ragged rows and keys,
-    one key tile only (the second warpgroup gets none), an odd number of
-    key tiles, and causal rows with no visible key (Sq > Skv)."""
+    take the key tiles in turn and merge their states (four with one K/V
+    stage at d = 32 and 64, two with two stages at d = 16); with more, and at
+    d = 128, one warpgroup per block does it all, with two stages while the
+    whole grid fits on the GPU at once and one stage beyond.  On 152 SMs:
+    B*H = 40 with 130 rows (200 blocks) takes two stages at d = 64 and one at
+    d = 128; B*H = 80 with 300 rows (800 blocks) takes one at every d.
+    Ragged rows and keys, one key tile only (the second warpgroup gets none),
+    an odd number of key tiles, and causal rows with no visible key
+    (Sq > Skv)."""
     B, H = bh
     q, k, v = f32(*qkv_inputs.normal_qkv(B, H, sq, skv, d, d + sq + skv + B * H))
     o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
