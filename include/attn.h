@@ -86,11 +86,13 @@ typedef enum attn_dtype {
  * run the tensor-core kernel with 128 x 128 tiles.
  * Requires a compute capability 10.3 device (GB300) for every dtype.
  *
- * CUDA graphs: the first call on a device sets up per-device state (kernel
- * attributes, the address of the status word).  After that a call only
- * enqueues one kernel on `stream` (two for attn_fwd_splitkv) and may be
+ * CUDA graphs: the first call that uses a kernel variant on a device sets
+ * up its per-device state (the kernel's shared-memory attribute, for the fp32
+ * kernel its occupancy, the address of the status word); the variant follows
+ * from dtype, d and the problem shape.  After that a call of the same shape
+ * only enqueues one kernel on `stream` (two for attn_fwd_splitkv) and may be
  * captured into a CUDA graph; a replay reads whatever the captured pointers
- * hold at replay time.  Make the first call before capturing.
+ * hold at replay time.  Make one ordinary call of the shape before capturing.
  */
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              int B, int H, int Sq, int Skv, int d, int causal, float scale,
