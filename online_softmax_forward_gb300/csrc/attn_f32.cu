@@ -591,10 +591,12 @@ int two_stage_blocks_per_sm() {
     return n;
 }
 
-// Fewer query blocks than SMs: several warpgroups per block split its key
-// tiles, so that each SM runs more warps -- four with one K/V stage each at
-// d = 32 and 64, two with two stages at d = 16 (where a warpgroup's state
-// would not fit one stage for the merge).  Otherwise one warpgroup per block:
+// Fewer query blocks than SMs and more than one key tile: several warpgroups
+// per block split its key tiles, so that each SM runs more warps -- four with
+// one K/V stage each at d = 32 and 64, two with two stages at d = 16 (where a
+// warpgroup's state would not fit one stage for the merge).  With one key
+// tile there is nothing to split and the merge would only cost (10.9 -> 8.9 us
+// at B=2, H=4, S=64, d=64).  Otherwise one warpgroup per block:
 // with two stages while the whole grid is resident at once, and with one
 // stage beyond that, which halves the block's K/V memory so that twice as
 // many blocks share an SM and hide one another's copies (+20 % at
@@ -606,8 +608,9 @@ int launch_tiled_d(const float *q, const float *k, const float *v, float *o, flo
     const int64_t grid = p.bh() * nqb;
     if (grid > INT32_MAX) return ATTN_ERR_INVALID_ARG;
     const int sms = device_sm_count();
+    const int key_tiles = (p.Skv + kTK - 1) / kTK;  // of the block that sees the most keys
     if constexpr (D <= 64) {
-        if (sms > 0 && grid < sms) {
+        if (sms > 0 && grid < sms && key_tiles > 1) {
             if constexpr (D >= 32) return launch_tiled_ks<D, 4, 1>(q, k, v, o, lse, p, grid, nqb, stream);
             return launch_tiled_ks<D, 2, 2>(q, k, v, o, lse, p, grid, nqb, stream);
         }

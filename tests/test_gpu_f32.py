@@ -137,16 +137,17 @@ def test_deterministic_and_lse_optional():
 @pytest.mark.parametrize("causal", [False, True])
 def test_attn_fwd_tiled_kernel(d, bh, sq, skv, causal):
     """attn_fwd's register-tiled kernel (32 query rows x 64 keys per tile).
-    With fewer query blocks than SMs (B*H = 2) several warpgroups per block
-    take the key tiles in turn and merge their states (four with one K/V
-    stage at d = 32 and 64, two with two stages at d = 16); with more, and at
-    d = 128, one warpgroup per block does it all, with two stages while the
-    whole grid fits on the GPU at once and one stage beyond.  On 152 SMs:
-    B*H = 40 with 130 rows (200 blocks) takes two stages at d = 64 and one at
-    d = 128; B*H = 80 with 300 rows (800 blocks) takes one at every d.
-    Ragged rows and keys, one key tile only (the second warpgroup gets none),
-    an odd number of key tiles, and causal rows with no visible key
-    (Sq > Skv)."""
+    With fewer query blocks than SMs (B*H = 2) and more than one key tile,
+    several warpgroups per block take the key tiles in turn and merge their
+    states (four with one K/V stage at d = 32 and 64, two with two stages at
+    d = 16); Skv = 300 and 130 give 5 and 3 key tiles, so some warpgroups get
+    one tile, one gets two, and with 3 tiles one gets none.  With one key tile
+    (Skv = 37), with more blocks, and at d = 128, one warpgroup per block does
+    it all, with two stages while the whole grid fits on the GPU at once and
+    one stage beyond.  On 152 SMs: B*H = 40 with 130 rows (200 blocks) takes
+    two stages at d = 64 and one at d = 128; B*H = 80 with 300 rows (800
+    blocks) takes one at every d.  Ragged rows and keys, and causal rows with
+    no visible key (Sq > Skv)."""
     B, H = bh
     q, k, v = f32(*qkv_inputs.normal_qkv(B, H, sq, skv, d, d + sq + skv + B * H))
     o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
