@@ -129,8 +129,10 @@ int attn_fwd_f32_blocked(const float *q, const float *k, const float *v,
  * host memory (one cudaMemcpyAsync per tensor, or per tensor and chunk).
  * Host buffers should be pinned for the copies to be asynchronous.  The call
  * returns after enqueueing; synchronise the stream before reading o_host.
- * Problems with at least 4 MiB of input are cut into 4 chunks of (batch,
- * head) slices that run on two streams the library creates once per device:
+ * Problems with at least 4 MiB of input are cut into up to 4 chunks of
+ * (batch, head) slices, with shares 2 : 3 : 3.5 : 1.5 (small first and last
+ * chunks, so the kernels start early and little is left after the last
+ * copy in), that run on two streams the library creates once per device:
  * the copies of one chunk overlap the kernel of the other.  Those streams
  * start after the work queued on `stream` and `stream` waits for them, so the
  * call behaves as if everything ran on `stream`; concurrent staged calls on

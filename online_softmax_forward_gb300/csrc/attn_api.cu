@@ -337,6 +337,22 @@ int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
     const size_t in_bytes = (nq + 2 * nkv) * ein;
     const int nchunks = (BH >= 2 && in_bytes >= kStagedMinBytes)
                             ? (int)(BH < kStagedChunks ? BH : kStagedChunks) : 1;
+    // chunk i holds the (batch, head) slices [bound[i], bound[i + 1]): shares
+    // in proportion to the weights, rounded, at least one slice each
+    int64_t bound[kStagedChunks + 1];
+    {
+        double total = 0.0, cum = 0.0;
+        for (int i = 0; i < nchunks; ++i) total += kStagedWeights[i];
+        bound[0] = 0;
+        for (int i = 1; i < nchunks; ++i) {
+            cum += kStagedWeights[i - 1];
+            int64_t b = (int64_t)((double)BH * cum / total + 0.5);
+            if (b < bound[i - 1] + 1) b = bound[i - 1] + 1;
+            if (b > BH - (nchunks - i)) b = BH - (nchunks - i);
+            bound[i] = b;
+        }
+        bound[nchunks] = BH;
+    }
     StagedStreams *res = nullptr;
     if (nchunks > 1) {
         res = staged_streams();
@@ -351,7 +367,7 @@ int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
     for (int i = 0; i < nchunks && err == ATTN_OK; ++i) {
         // (batch, head) slices [b0, b1) on alternating streams: the copies of
         // one chunk overlap the kernel and the copies of the other
-        const int64_t b0 = BH * i / nchunks, b1 = BH * (i + 1) / nchunks;
+        const int64_t b0 = bound[i], b1 = bound[i + 1];
         cudaStream_t cs = nchunks > 1 ? res->st[i & 1] : s;
         const size_t oq = (size_t)b0 * Sq * d, okv = (size_t)b0 * Skv * d;
         const size_t cq = (size_t)(b1 - b0) * Sq * d, ckv = (size_t)(b1 - b0) * Skv * d;

@@ -69,12 +69,15 @@ bool set_smem_limit_once(const void *func, int bytes);
 int device_sm_count();
 
 // Host-staged calls (attn_fwd_staged) of at least kStagedMinBytes of input
-// run in kStagedChunks chunks of (batch, head) slices on two library streams
-// of the device, so that copies overlap the kernels.
-#ifndef ATTN_STAGED_CHUNKS
-#define ATTN_STAGED_CHUNKS 4
-#endif
-constexpr int kStagedChunks = ATTN_STAGED_CHUNKS;
+// run in chunks of (batch, head) slices on two library streams of the
+// device, so that copies overlap the kernels.  Chunk i takes a share of the
+// slices in proportion to kStagedWeights[i] (fewer chunks when there are
+// fewer slices).  A small first chunk starts the kernels early; a small last
+// chunk shortens what is left after the last host-to-device copy (its kernel
+// and its copy back); the shares grow in between so that each copy lands
+// before the kernel before it ends.
+constexpr double kStagedWeights[] = {2.0, 3.0, 3.5, 1.5};
+constexpr int kStagedChunks = (int)(sizeof(kStagedWeights) / sizeof(kStagedWeights[0]));
 constexpr size_t kStagedMinBytes = (size_t)4 << 20;
 struct StagedStreams {
     cudaStream_t st[2];

@@ -205,9 +205,10 @@ def test_staged_host_buffers_match_device_call():
     (2, 3, 600, 600, 64, False, torch.float32),
 ])
 def test_staged_chunked_matches_device_call(case):
-    """Large host-staged calls are cut into chunks of (batch, head) slices on
-    two library streams; the result is the same as the device call, and work
-    queued on the caller's stream afterwards sees it complete."""
+    """Large host-staged calls are cut into up to four chunks of (batch, head)
+    slices of unequal sizes (16 slices: 3, 5, 6, 2; 5: 1, 2, 1, 1; 6: 1, 2,
+    2, 1) on two library streams; the result is the same as the device call,
+    and work queued on the caller's stream afterwards sees it complete."""
     ensure_built()
     B, H, Sq, Skv, d, causal, dt = case
     q, k, v = (t.to(dt) for t in qkv_inputs.normal_qkv(B, H, Sq, Skv, d, seed=Sq + H))
