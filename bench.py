@@ -53,9 +53,15 @@ CONFIGS = {
     "b1_h32_s8192_d128_fp16_causal": (1, 32, 8192, 8192, 128, True, "f16", "normal"),
     "b1_h64_s8192_d64_bf16_causal": (1, 64, 8192, 8192, 64, True, "bf16", "normal"),
     "b1_h32_s8192_d128_bf16_full": (1, 32, 8192, 8192, 128, False, "bf16", "normal"),
+    # sequence-sharded: the keys in 4 contiguous shards, as separate devices would hold
+    # them; attn_fwd on each shard (fp32 partial O and LSE), then attn_merge
+    "b1_h32_s8192_d128_bf16_full_kv4shards": (1, 32, 8192, 8192, 128, False, "bf16", "normal"),
 }
 # few query rows against many keys: the split-KV path (partial kernel + merge)
 SPLITKV = {"b4_h32_q1_kv32768_d128_bf16_decode", "b1_h1_q8_kv1024_d32_f32"}
+# sequence-sharded workloads: number of key shards (non-causal only: a causal mask
+# does not split into per-shard bottom-right masks)
+SHARDED = {"b1_h32_s8192_d128_bf16_full_kv4shards": 4}
 # fp32 workloads whose arithmetic, not their bytes, bounds them (about 128 FLOP per byte)
 FP32_ALU = {"b2_h4_s512_d64_f32"}
 FP32_FMA_PER_CLK_PER_SM = 128  # CUDA-core FP32 lanes of one SM
@@ -231,6 +237,16 @@ def run_gpu(args, rank, world, local_rank):
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
     splitkv = args.config in SPLITKV
+    n_shards = SHARDED.get(args.config, 0)
+    if n_shards:
+        # each shard contiguous, as on its own device; fp32 partials [n, B, H, Sq, (d)]
+        sk = Skv // n_shards
+        k_sh = [k[:, :, i * sk:(i + 1) * sk].contiguous() for i in range(n_shards)]
+        v_sh = [v[:, :, i * sk:(i + 1) * sk].contiguous() for i in range(n_shards)]
+        o_parts = torch.empty((n_shards, B, H, Sq, d), dtype=torch.float32, device=dev)
+        lse_parts = torch.empty((n_shards, B, H, Sq), dtype=torch.float32, device=dev)
+        part_code = {"bf16": pkg.ATTN_BF16_OUT_F32, "f16": pkg.ATTN_F16_OUT_F32,
+                     "f32": pkg.ATTN_F32}[dt]
     n_splits, ws = 0, None
     if splitkv:
         st, n_splits, ws_bytes = pkg.attn_splitkv_plan(B, H, Sq, Skv, d, code)
@@ -238,7 +254,22 @@ def run_gpu(args, rank, world, local_rank):
             raise pkg.AttnError(st, "attn_splitkv_plan")
         ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
+    def launch_sharded(qq, ks, vs):
+        for i in range(n_shards):
+            st = pkg.attn_fwd(qq.data_ptr(), ks[i].data_ptr(), vs[i].data_ptr(),
+                              o_parts[i].data_ptr(), lse_parts[i].data_ptr(), B, H, Sq, sk, d,
+                              0, 0.0, part_code, sh)
+            if st != pkg.ATTN_OK:
+                raise pkg.AttnError(st, "attn_fwd (shard)")
+        st = pkg.attn_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n_shards, B * H * Sq, d,
+                            o.data_ptr(), lse.data_ptr(), code, sh)
+        if st != pkg.ATTN_OK:
+            raise pkg.AttnError(st, "attn_merge")
+
     def launch(qq=q, kk=k, vv=v):
+        if n_shards:
+            launch_sharded(qq, k_sh if kk is k else kk, v_sh if vv is v else vv)
+            return
         if splitkv:
             st = pkg.attn_fwd_splitkv(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
                                       lse.data_ptr(), B, H, Sq, Skv, d, int(causal), 0.0, code,
@@ -284,6 +315,11 @@ def run_gpu(args, rank, world, local_rank):
 
     # e2e: host buffers through attn_fwd_staged, copies inside the timed region
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    if n_shards:
+        kh_sh = [t.cpu().pin_memory() for t in k_sh]
+        vh_sh = [t.cpu().pin_memory() for t in v_sh]
+        dk_sh = [torch.empty_like(t) for t in k_sh]
+        dv_sh = [torch.empty_like(t) for t in v_sh]
     oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
@@ -293,7 +329,14 @@ def run_gpu(args, rank, world, local_rank):
             flush.fill_(i & 0xFF)
             stream.synchronize()
             t0 = time.perf_counter()
-            if splitkv:  # host -> device copies, the split-KV call, device -> host copies
+            if n_shards:  # host -> device copies of q and every shard, the shards, the merge
+                dq.copy_(qh, non_blocking=True)
+                for dst, src_ in zip(dk_sh + dv_sh, kh_sh + vh_sh):
+                    dst.copy_(src_, non_blocking=True)
+                launch(dq, dk_sh, dv_sh)
+                oh.copy_(o, non_blocking=True)
+                lh.copy_(lse, non_blocking=True)
+            elif splitkv:  # host -> device copies, the split-KV call, device -> host copies
                 for dst, src_ in ((dq, qh), (dk, kh), (dv, vh)):
                     dst.copy_(src_, non_blocking=True)
                 launch(dq, dk, dv)
@@ -317,7 +360,8 @@ def run_gpu(args, rank, world, local_rank):
     # max over ranks of the per-step device time
     ms_max, e2e_s = max_over_ranks([ms, sum(e2e_times) / len(e2e_times)], world, dev)
     return dict(ms=ms_max, flops=f, times=times, wall=wall, clocks=clocks, e2e_s=e2e_s,
-                h2d=h2d, d2h=d2h, cfg=cfg, launches_per_step=2 if splitkv else 1,
+                h2d=h2d, d2h=d2h, cfg=cfg,
+                launches_per_step=n_shards + 1 if n_shards else (2 if splitkv else 1),
                 n_splits=n_splits)
 
 
@@ -412,7 +456,9 @@ def main(argv=None):
     B, H, Sq, Skv, d, causal, dt, _ = cfg
     peaks = load_peaks()
     config = {"workload": args.config, "B": B, "H": H, "Sq": Sq, "Skv": Skv, "d": d,
-              "path": "split-KV (attn_fwd_splitkv)" if args.config in SPLITKV else "attn_fwd",
+              "path": ("split-KV (attn_fwd_splitkv)" if args.config in SPLITKV else
+                       "sequence-sharded: attn_fwd on %d key shards (fp32 partials) + attn_merge"
+                       % SHARDED[args.config] if args.config in SHARDED else "attn_fwd"),
               "causal": causal, "inputs": "iid standard normal, seeded" if cfg[7] == "normal"
               else "iid uniform(-0.8,0.8), random.Random(42)",
               "l2": "flushed between steps (256 MiB fill outside the kernel events)",

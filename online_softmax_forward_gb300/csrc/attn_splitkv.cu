@@ -358,10 +358,10 @@ splitkv_partial_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
     }
 }
 
-// One CTA of kMergeThreads per row: merges n_parts partial results
-// [n_parts][rows][d] / [n_parts][rows] into o [rows][d] and lse [rows].  The
-// weights exp(lse_p - M) are computed once into shared memory; each thread
-// then sums its columns over the parts.
+// Merge of n_parts partial results [n_parts][rows][d] / [n_parts][rows] into
+// o [rows][d] and lse [rows].  merge_kernel, for more than 32 parts: one CTA
+// of kMergeThreads per row; the weights exp(lse_p - M) are computed once
+// into shared memory; each thread then sums its columns over the parts.
 constexpr int kMergeThreads = 128;
 
 __device__ __forceinline__ float block_reduce(float x, float *red, bool is_max) {
@@ -418,23 +418,79 @@ merge_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_p
     if (lse && threadIdx.x == 0) lse[row] = M + logf(L);
 }
 
+// One warp per row, for up to 32 parts: lane p holds the weight of part p,
+// the lanes split the columns, so each part's row is one coalesced read and
+// no block barrier is needed.  With many rows (the heads and queries of a
+// sequence-sharded prefill: 262,144 rows) this runs at memory speed, where
+// one CTA per row spends its time on CTA scheduling and block reductions.
+// The sums are taken in the same order as merge_kernel's, so both give the
+// same bits.
+constexpr int kMergeRowWarps = 8;  // rows per CTA
+
+template <typename TO>
+__global__ void __launch_bounds__(kMergeRowWarps * 32)
+merge_rows_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_parts,
+                  int64_t rows, int d, TO *__restrict__ o, float *__restrict__ lse) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * kMergeRowWarps + (threadIdx.x >> 5);
+    if (row >= rows) return;  // the whole warp: one row per warp
+    const float lp = lane < n_parts ? pl[(int64_t)lane * rows + row] : -INFINITY;
+    const float M = warp_max(lp);
+    TO *orow = o + row * d;
+    if (M == -INFINITY) {  // no part saw a key: o = 0, lse = -inf
+        for (int c = lane; c < d; c += 32) orow[c] = from_f32<TO>(0.f);
+        if (lse && lane == 0) lse[row] = -INFINITY;
+        return;
+    }
+    const float w = lp == -INFINITY ? 0.f : expf(lp - M);  // a part with no key weighs 0
+    const float L = warp_sum(w);
+    const float inv = 1.f / L;
+    const float *prow = po + row * d;
+    const int64_t pstride = rows * d;
+    for (int c0 = 0; c0 < d; c0 += 128) {  // four columns per lane in flight
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int q = 0; q < n_parts; ++q) {
+            const float wq = __shfl_sync(0xffffffffu, w, q);
+            if (wq == 0.f) continue;  // the same for the whole warp
+            const float *col = prow + (int64_t)q * pstride;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + lane + 32 * u;
+                if (c < d) a[u] = fmaf(wq, col[c], a[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + lane + 32 * u;
+            if (c < d) orow[c] = from_f32<TO>(a[u] * inv);
+        }
+    }
+    if (lse && lane == 0) lse[row] = M + logf(L);
+}
+
 template <typename TO>
 int launch_merge_t(const float *po, const float *pl, int n_parts, int64_t rows, int d, void *o,
                    float *lse, cudaStream_t stream) {
     if (rows == 0) return ATTN_OK;
     if (rows > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+    const bool by_warp = n_parts <= 32;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)rows);
-    cfg.blockDim = dim3(kMergeThreads);
-    cfg.dynamicSmemBytes = (size_t)n_parts * sizeof(float);
+    cfg.gridDim = dim3(by_warp ? (unsigned)((rows + kMergeRowWarps - 1) / kMergeRowWarps)
+                               : (unsigned)rows);
+    cfg.blockDim = dim3(by_warp ? kMergeRowWarps * 32 : kMergeThreads);
+    cfg.dynamicSmemBytes = by_warp ? 0 : (size_t)n_parts * sizeof(float);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel<TO>, po, pl, n_parts, rows, d,
-                                             reinterpret_cast<TO *>(o), lse);
+    const cudaError_t e =
+        by_warp ? cudaLaunchKernelEx(&cfg, merge_rows_kernel<TO>, po, pl, n_parts, rows, d,
+                                     reinterpret_cast<TO *>(o), lse)
+                : cudaLaunchKernelEx(&cfg, merge_kernel<TO>, po, pl, n_parts, rows, d,
+                                     reinterpret_cast<TO *>(o), lse);
     return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 

@@ -75,3 +75,15 @@ def test_kernel_hash_ignores_comments_only():
     c = "int f(int x) { return x + 2; }"
     assert bench.code_only(a) == bench.code_only(b)
     assert bench.code_only(a) != bench.code_only(c)
+
+
+def test_sharded_workloads_split_evenly_and_are_not_causal():
+    """A bottom-right causal mask does not split into per-shard masks, and
+    the bench cuts the keys into equal contiguous shards."""
+    assert bench.SHARDED
+    for name, n in bench.SHARDED.items():
+        B, H, Sq, Skv, d, causal, dt, _ = bench.CONFIGS[name]
+        assert not causal and n >= 2 and Skv % n == 0
+        assert name not in bench.SPLITKV
+        # the dominant kernel is the tensor-core kernel of the shards
+        assert bench.kernel_source_hash(name) == bench.kernel_source_hash(bench.DEFAULT)

@@ -171,6 +171,81 @@ def test_merge_of_key_shards(bounds, out_dtype):
     assert np.abs(lm.double().cpu().numpy() - lse_ref).max() <= 1e-5
 
 
+def _sharded(qd, kd, vd, bounds, out_dtype):
+    """Sequence-sharded attention as the bench's sharded workload runs it:
+    each key shard contiguous (as on its own device), the tensor-core kernel
+    on each with fp32 partial O and LSE, then attn_merge."""
+    po, pl = [], []
+    d = qd.shape[-1]
+    for a, b in bounds:
+        o, lse = pkg.attention(qd, kd[:, :, a:b].contiguous(), vd[:, :, a:b].contiguous(),
+                               out_dtype=torch.float32)
+        po.append(o.reshape(-1, d))
+        pl.append(lse.reshape(-1))
+    om, lm = pkg.merge(torch.stack(po), torch.stack(pl), out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert pkg.attn_check_status(None) == pkg.ATTN_OK
+    return om, lm
+
+
+@pytest.mark.parametrize("case", [
+    # B, H, Sq, Skv, d, shard bounds
+    (1, 4, 1024, 4096, 128, [(0, 1024), (1024, 2048), (2048, 3072), (3072, 4096)]),
+    (2, 3, 300, 1000, 64, [(0, 333), (333, 666), (666, 1000)]),
+    (1, 2, 129, 515, 128, [(0, 128), (128, 129), (129, 515)]),
+])
+def test_sequence_sharded_bf16_matches_oracle(case):
+    """bf16 inputs, keys in contiguous shards (equal, unequal, one of a
+    single key), the tensor-core kernel per shard, the merge to fp32 and to
+    bf16 output: every row against the fp64 oracle over all keys, with the
+    16-bit-input tolerances."""
+    ensure_built()
+    B, H, Sq, Skv, d, bounds = case
+    q, k, v = qkv_inputs.normal_qkv(B, H, Sq, Skv, d, seed=Skv + H, dtype=torch.bfloat16)
+    o_ref, lse_ref = oracle.attention(q, k, v)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o_ref, lse_ref = o_ref.reshape(-1, d), lse_ref.reshape(-1)
+    om, lm = _sharded(qd, kd, vd, bounds, torch.float32)
+    assert_bf16_parity(om.double().cpu().numpy(), lm.double().cpu().numpy(), o_ref, lse_ref)
+    ob, lb = _sharded(qd, kd, vd, bounds, torch.bfloat16)
+    assert_rounded_output(ob.double().cpu().numpy(), o_ref, torch.bfloat16)
+    assert torch.equal(lb, lm)
+
+
+def test_sequence_sharded_b1_h32_s8192_sampled():
+    """The bench's sharded workload at full size (B=1, H=32, Sq=Skv=8192,
+    d=128, bf16, four shards of 2048 keys): every row finite; stratified rows
+    of four heads against the oracle over all keys; and every row within the
+    sum of both bounds of the unsharded attn_fwd."""
+    ensure_built()
+    B, H, S, d = 1, 32, 8192, 128
+    q, k, v = qkv_inputs.normal_qkv(B, H, S, S, d, seed=0, dtype=torch.bfloat16)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    bounds = [(i * 2048, (i + 1) * 2048) for i in range(4)]
+    om, lm = _sharded(qd, kd, vd, bounds, torch.float32)
+    assert torch.isfinite(om).all() and torch.isfinite(lm).all()
+    o_whole, l_whole = pkg.attention(qd, kd, vd, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    # both are held to the oracle bounds, so they differ by at most their sum
+    assert (om.reshape(B, H, S, d) - o_whole).abs().max().item() <= 2e-2
+    assert (lm.reshape(B, H, S) - l_whole).abs().max().item() <= 2e-4 * max(
+        1.0, l_whole.abs().max().item())
+    qh, kh, vh = (t.reshape(B * H, S, d) for t in (q, k, v))
+    omh = om.reshape(B * H, S, d).double().cpu().numpy()
+    lmh = lm.reshape(B * H, S).double().cpu().numpy()
+    got, got_l, refs, ref_l = [], [], [], []
+    for bh in (0, 11, 22, 31):
+        rs = qkv_inputs.sample_rows(S, 16, seed=2000 + bh)
+        o_b, l_b = oracle.attention_rows(qh[bh:bh + 1], kh[bh:bh + 1], vh[bh:bh + 1],
+                                         [(0, i) for i in rs])
+        got.append(omh[bh, rs])
+        got_l.append(lmh[bh, rs])
+        refs.append(o_b)
+        ref_l.append(l_b)
+    assert_bf16_parity(np.concatenate(got), np.concatenate(got_l), np.concatenate(refs),
+                       np.concatenate(ref_l))
+
+
 def test_merge_empty_parts():
     ensure_built()
     po = torch.randn(3, 4, 32, device="cuda")
