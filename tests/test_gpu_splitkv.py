@@ -73,6 +73,23 @@ def test_shapes_fp32(case, n_splits):
     assert_f32_parity(o, lse, o_ref, lse_ref)
 
 
+@pytest.mark.parametrize("n_splits", [40, 64, 256])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_more_than_32_splits(n_splits, out_dtype):
+    """More than 32 partial results per row: the merge runs one CTA per row
+    (up to 32 it runs one warp per row).  5000 keys in splits of a multiple
+    of 32 keys give 40, 53 and 157 parts."""
+    q, k, v = qkv_inputs.normal_qkv(1, 2, 3, 5000, 64, seed=n_splits, dtype=torch.bfloat16)
+    o_ref, lse_ref = oracle.attention(q, k, v)
+    o, lse = run_split(q, k, v, False, dtype=torch.bfloat16, out_dtype=out_dtype,
+                       n_splits=n_splits)
+    if out_dtype == torch.float32:
+        assert_bf16_parity(o, lse, o_ref, lse_ref)
+    else:
+        assert_rounded_output(o, o_ref, torch.bfloat16)
+        assert_lse_close(lse, lse_ref, 1e-4)
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("case", [
     (2, 4, 1, 4096, 128, False),
@@ -142,7 +159,9 @@ def test_plan_fills_the_device():
 
 # ------------------------------------------------------------------ merge
 @pytest.mark.parametrize("bounds", [[(0, 100), (100, 101), (101, 777)],
-                                    [(500, 777), (0, 500)], [(0, 777)]])
+                                    [(500, 777), (0, 500)], [(0, 777)],
+                                    # 41 parts: the one-CTA-per-row merge
+                                    [(19 * i, 19 * i + 19) for i in range(40)] + [(760, 777)]])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_merge_of_key_shards(bounds, out_dtype):
     """Partial results over key shards (computed by attn_fwd on each shard)
