@@ -13,8 +13,10 @@
 // block raises the running maximum:
 //     M = max_s lse_s,  w_s = exp(lse_s - M),  o = sum_s w_s o_s / sum_s w_s,
 //     lse = M + ln(sum_s w_s).
-// The merge kernel is also exported on its own (attn_merge), for results
-// computed over key shards elsewhere.
+// The merge is also exported on its own (attn_merge), for results computed
+// over key shards elsewhere.  Up to 32 parts it runs one warp per row (8 rows
+// per CTA, lane s holds w_s, the lanes split the columns); beyond that, one
+// CTA per row.
 //
 // Partial kernel: CTA (bh, split, block of RB query rows).  Each warp walks
 // its own 32-key tiles of the split (tiles warp, warp + W, ...), staged in
