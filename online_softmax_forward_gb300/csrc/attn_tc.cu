@@ -20,7 +20,8 @@
 //  * Warps 9 and 10 issue the tcgen05.mma (kind::f16, fp32 accumulate) of
 //    query tile 0 and 1 respectively, as whole warps with one elected lane:
 //        S_t = Q_t K_j^T  (shared-memory operands, fp32 result in TMEM)
-//        O_t += P_t V_j   (P_t and V_j in shared memory, O_t in TMEM)
+//        O_t += P_t V_j   (V_j in shared memory, O_t in TMEM; P_t in shared
+//                          memory at d = 128, in TMEM at d = 64)
 //    S_t(j+1) is issued as soon as the softmax has copied S_t(j) out of tensor
 //    memory, so the tensor core computes the next scores while the softmax
 //    exponentiates the current ones; PV_t(j) follows once P_t(j) is written.
@@ -31,13 +32,15 @@
 //    max; at d = 64 both are in flight at once), apply the causal / tail
 //    mask, take the row max, exponentiate with
 //    ex2 (scores pre-multiplied by scale*log2 e, paired fp32 arithmetic), sum,
-//    and write P as 16-bit values into a shared-memory tile in the MMA's
-//    128-byte-swizzled layout.  The running max is updated lazily: O and l are
+//    and write P as 16-bit values: at d = 128 into a shared-memory tile in the
+//    MMA's 128-byte-swizzled layout, at d = 64 into tensor memory with two
+//    32-column stores (no swizzle, no proxy fence; 7-9 % faster).  The running max is updated lazily: O and l are
 //    rescaled (O in TMEM, after the previous P.V has completed) only when the
 //    max grows by more than 2^8, so P stays <= 256; O, l and m always refer
 //    to the same stale max, so the result is the same softmax.  After the
 //    last tile they write O / l and lse = m + ln l.
-//  * Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0, O1 after.
+//  * Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0, O1 after;
+//    at d = 64 also P0 [384,448) and P1 [448,512), 16-bit pairs per column.
 //  * Every mbarrier wait is bounded (globaltimer).  On expiry the CTA sets an
 //    abort flag, records ATTN timeout in the status word, lets every role
 //    leave its loop, waits for its own TMA loads and MMAs in flight, frees
@@ -80,15 +83,19 @@ struct Cfg {
     static constexpr int kChunkBytes = BN * 128;      // one atom column of a 128-row tile: 16 KB
     static constexpr int kTileBytes = kChunks * kChunkBytes;  // Q, K or V tile
     static constexpr int kPBytes = 2 * kChunkBytes;   // P tile: 128 rows x 128 keys, 16-bit
+    // at d = 64 tensor memory has room for P next to S and O: P_t in columns
+    // 384 + 64 t, and the P.V MMAs read it from there
+    static constexpr bool kTmemP = D == 64;
     static constexpr int kStages = D == 128 ? 3 : 6;  // K/V ring depth (fills 227 KB)
     static constexpr int kOffQ = 0;                   // Q0, Q1
-    static constexpr int kOffP = 2 * kTileBytes;      // P0, P1
-    static constexpr int kOffKV = kOffP + 2 * kPBytes;  // ring stages
+    static constexpr int kOffP = 2 * kTileBytes;      // P0, P1 (shared memory at d = 128)
+    static constexpr int kOffKV = kOffP + (kTmemP ? 0 : 2 * kPBytes);  // ring stages
     static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
     static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
     // tensor-memory columns of S_t and O_t
     __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
     __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? (uint32_t)D : 0u); }
+    __device__ static constexpr uint32_t col_p(int t) { return 384u + (t ? 64u : 0u); }
 };
 constexpr int kMaxStages = 6;
 
@@ -486,11 +493,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             ptx::tc_fence_after();
             const uint64_t dvj = dv + (uint64_t)((st * C::kTileBytes) >> 4);
+            if constexpr (C::kTmemP) {
+                // A = P_t from tensor memory: 16 keys (8 columns of bf16 pairs) per MMA
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint32_t koff = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-                ptx::mma_ss_warp(tO, dp + koff, dvj + (uint64_t)((kk * 16 * 128) >> 4), kIdescO,
-                                 (jj > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    ptx::mma_ts_warp(tO, tmem + C::col_p(t) + kk * 8,
+                                     dvj + (uint64_t)((kk * 16 * 128) >> 4), kIdescO,
+                                     (jj > 0 || kk > 0) ? 1u : 0u);
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint32_t koff = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+                    ptx::mma_ss_warp(tO, dp + koff, dvj + (uint64_t)((kk * 16 * 128) >> 4),
+                                     kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
+                }
             }
             ptx::mma_commit_warp(bar(bars->p_free[t]));
             ptx::mma_commit_warp(bar(bars->kv_empty[st]));
@@ -530,6 +546,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t tS = tmem + lane_base + C::col_s(t);
         const uint32_t tO = tmem + lane_base + C::col_o(t);
         const uint32_t pRow = sP + t * C::kPBytes + r * 128;  // this row in both P atom columns
+        const uint32_t tP = tmem + lane_base + C::col_p(t);  // this warp's lanes of P_t (d = 64)
         const uint32_t swz = (uint32_t)(r & 7);               // 128-byte swizzle phase of the row
         const float sl2 = p.scale_log2;
         const int off = p.Skv - p.Sq;
@@ -629,19 +646,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     ++pfn;
                     if (!__all_sync(0xffffffffu, g2)) { ok = false; break; }
                 }
-                // P row into the K-major, 128-byte-swizzled tile: 16-byte chunk c
-                // of a 128-byte row is stored at chunk c ^ (row mod 8)
+                if constexpr (C::kTmemP) {
+                    // P row into tensor memory: column c holds keys 2c, 2c + 1
+                    ptx::tmem_st32(tP, pa);
+                    exp32<kBF16>(rb.a, sl2, mb, pb, acc);
+                    exp32<kBF16>(rb.b, sl2, mb, pb + 16, acc);
+                    ptx::tmem_st32(tP + 32, pb);
+                    ptx::tmem_wait_st();
+                } else {
+                    // P row into the K-major, 128-byte-swizzled tile: 16-byte chunk c
+                    // of a 128-byte row is stored at chunk c ^ (row mod 8)
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    ptx::st_shared_v4(pRow + ((((uint32_t)c) ^ swz) << 4), pa[4 * c], pa[4 * c + 1],
-                                      pa[4 * c + 2], pa[4 * c + 3]);
-                exp32<kBF16>(rb.a, sl2, mb, pb, acc);
-                exp32<kBF16>(rb.b, sl2, mb, pb + 16, acc);
+                    for (int c = 0; c < 8; ++c)
+                        ptx::st_shared_v4(pRow + ((((uint32_t)c) ^ swz) << 4), pa[4 * c],
+                                          pa[4 * c + 1], pa[4 * c + 2], pa[4 * c + 3]);
+                    exp32<kBF16>(rb.a, sl2, mb, pb, acc);
+                    exp32<kBF16>(rb.b, sl2, mb, pb + 16, acc);
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    ptx::st_shared_v4(pRow + C::kChunkBytes + ((((uint32_t)c) ^ swz) << 4), pb[4 * c],
-                                      pb[4 * c + 1], pb[4 * c + 2], pb[4 * c + 3]);
-                ptx::fence_proxy_async_smem();
+                    for (int c = 0; c < 8; ++c)
+                        ptx::st_shared_v4(pRow + C::kChunkBytes + ((((uint32_t)c) ^ swz) << 4),
+                                          pb[4 * c], pb[4 * c + 1], pb[4 * c + 2], pb[4 * c + 3]);
+                    ptx::fence_proxy_async_smem();
+                }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(bars->p_full[t]));
                 const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
