@@ -35,6 +35,20 @@ def test_p1_printed_sample_rows():
     assert np.array_equal(o[0], np.asarray(v[0]))
 
 
+@pytest.mark.parametrize("seed", [42, 7])
+def test_uniform_generator_is_the_pages_make_qkv(seed):
+    """The array generator used for the single-head and decode-like inputs
+    draws exactly what aiml.sh "verify-tiled-attention" make_qkv draws: with
+    one (batch, head) slice and Sq = Skv it returns the same q, k and v,
+    element for element, as the page's list generator (whose seed-42 output
+    the printed sample rows pin above)."""
+    q_l, k_l, v_l = qkv_inputs.make_qkv(64, 16, seed)
+    q, k, v = qkv_inputs.uniform_qkv(1, 1, 64, 64, 16, seed)
+    for arr, lists in ((q, q_l), (k, k_l), (v, v_l)):
+        assert arr.shape == (1, 1, 64, 16)
+        assert np.array_equal(arr[0, 0], np.asarray(lists, dtype=np.float64))
+
+
 def test_p1_retained_element_count():
     """The page's dense reference keeps 4160 score+probability elements for
     causal N=64, i.e. 2080 visible (query, key) pairs.  With q = 0 every
