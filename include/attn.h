@@ -58,6 +58,15 @@ extern "C" {
 
 #define ATTN_ABI_VERSION 1
 
+/* The library is built with hidden visibility; only the functions declared
+ * with ATTN_API (this header's) are exported.  The test-only entry points
+ * (attn_test.h) are exported by libattn_test.so alone. */
+#if defined(__GNUC__) || defined(__clang__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
 typedef enum attn_status {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,        /* null/misaligned/overlapping pointer, bad size or dtype */
@@ -65,7 +74,9 @@ typedef enum attn_status {
     ATTN_ERR_LAUNCH = 3,             /* a CUDA launch or copy failed */
     ATTN_ERR_TIMEOUT = 4,            /* a kernel's bounded wait expired (see attn_check_status) */
     ATTN_ERR_CUDA = 5,               /* another CUDA runtime/driver error */
-    ATTN_ERR_SCRATCH_LIMIT = 6       /* attn_fwd_splitkv_noalloc: problem exceeds its fixed scratch */
+    ATTN_ERR_SCRATCH_LIMIT = 6,      /* attn_fwd_splitkv_noalloc: problem exceeds its fixed scratch */
+    ATTN_ERR_BOUNDS = 7              /* bounds-checking build only: an index check failed and the
+                                        access was skipped (see attn_check_status) */
 } attn_status;
 
 typedef enum attn_dtype {
@@ -94,7 +105,7 @@ typedef enum attn_dtype {
  * captured into a CUDA graph; a replay reads whatever the captured pointers
  * hold at replay time.  Make one ordinary call of the shape before capturing.
  */
-int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              int B, int H, int Sq, int Skv, int d, int causal, float scale,
              int dtype, void *stream);
 
@@ -103,24 +114,9 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  * call or launch.  Returns ATTN_OK or ATTN_ERR_INVALID_ARG.  Pointers are only
  * compared and tested for alignment, never dereferenced.
  */
-int attn_validate(const void *q, const void *k, const void *v, const void *o,
+ATTN_API int attn_validate(const void *q, const void *k, const void *v, const void *o,
                   const float *lse, int B, int H, int Sq, int Skv, int d,
                   int causal, float scale, int dtype);
-
-/*
- * attn_fwd_f32_blocked -- the fp32 CUDA-core path with caller-chosen tile
- * sizes, so that block-size invariance (including sizes that do not divide
- * the sequence, e.g. 7, or 13 x 19) can be tested as the pages do
- * (aiml.sh "verify-tiled-attention" test_lab.py tile sweep; huhohoo
- * "tiled-online-softmax" exercise with block size seven).
- * block_q in [1, 128], block_kv in [1, 256]; the key tile must fit in shared
- * memory (ATTN_ERR_INVALID_ARG otherwise).  Other arguments as attn_fwd with
- * dtype ATTN_F32.
- */
-int attn_fwd_f32_blocked(const float *q, const float *k, const float *v,
-                         float *o, float *lse, int B, int H, int Sq, int Skv,
-                         int d, int causal, float scale, int block_q,
-                         int block_kv, void *stream);
 
 /*
  * attn_fwd_staged -- attn_fwd on HOST buffers: copies q, k, v from host memory
@@ -141,7 +137,7 @@ int attn_fwd_f32_blocked(const float *q, const float *k, const float *v,
  * Sizes and dtype as attn_fwd; host pointers must not be NULL when their
  * tensor is non-empty.
  */
-int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
+ATTN_API int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
                     void *o_host, float *lse_host, void *dq, void *dk, void *dv,
                     void *do_, float *dlse, int B, int H, int Sq, int Skv,
                     int d, int causal, float scale, int dtype, void *stream);
@@ -167,7 +163,7 @@ int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
  * [n_splits][B*H][Sq][d] followed by partial lse [n_splits][B*H][Sq], fp32).
  * Host only.  d in {16, 32, 64, 128}; 1 <= n_splits <= 256.
  */
-int attn_splitkv_workspace_size(int B, int H, int Sq, int d, int n_splits, size_t *bytes);
+ATTN_API int attn_splitkv_workspace_size(int B, int H, int Sq, int d, int n_splits, size_t *bytes);
 
 /*
  * attn_splitkv_plan -- the split count the library would pick on the current
@@ -177,7 +173,7 @@ int attn_splitkv_workspace_size(int B, int H, int Sq, int d, int n_splits, size_
  * fixed cost per CTA (about two tiles), with at least two tiles per warp in
  * each split.  Needs a compute capability 10.3 device.
  */
-int attn_splitkv_plan(int B, int H, int Sq, int Skv, int d, int dtype, int *n_splits,
+ATTN_API int attn_splitkv_plan(int B, int H, int Sq, int Skv, int d, int dtype, int *n_splits,
                       size_t *workspace_bytes);
 
 /*
@@ -196,7 +192,7 @@ int attn_splitkv_plan(int B, int H, int Sq, int Skv, int d, int dtype, int *n_sp
  * ATTN_ERR_INVALID_ARG for a missing, small, misaligned or overlapping
  * workspace; otherwise as attn_fwd.
  */
-int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+ATTN_API int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
                      int B, int H, int Sq, int Skv, int d, int causal, float scale,
                      int dtype, int n_splits, void *workspace, size_t workspace_bytes,
                      void *stream);
@@ -211,15 +207,21 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float
  *
  * Instead of a caller-provided workspace it uses a scratch array of
  * ATTN_NOALLOC_SCRATCH_BYTES (8 MiB) that is part of the library's device
- * image: every GPU that loads the library holds it until the process exits.
- * The call itself allocates nothing and calls no allocating routine.
+ * image: every GPU on which the library is used holds it until the process
+ * exits.  The call calls no allocating routine (no cudaMalloc, no library
+ * allocator).
  *   - Size limit: the problem must fit, i.e.
  *     4 * n_splits * B * H * Sq * (d + 1) <= ATTN_NOALLOC_SCRATCH_BYTES
- *     (see attn_splitkv_workspace_size); otherwise ATTN_ERR_SCRATCH_LIMIT is
- *     returned before anything is launched.
- *   - First call on a device: it looks up the array's device address once
- *     for that device (with that device current).  Make that first call
- *     before capturing a stream.
+ *     (see attn_splitkv_workspace_size) whenever Skv > 0; otherwise
+ *     ATTN_ERR_SCRATCH_LIMIT is returned before anything is launched.
+ *   - Set-up on a device: the first call of ANY entry point on a device
+ *     (with that device current) looks up the array's device address, which
+ *     makes CUDA load the module holding it and reserve the 8 MiB there.  The
+ *     first launch of each kernel variant may also make the driver load that
+ *     kernel's code.  Both happen once per device; so, before entering code
+ *     that must not allocate, make one call of this entry point on the
+ *     device with the same dtype and head width (and before capturing a
+ *     stream).  Later calls change nothing in the device's free memory.
  *   - Sharing: every call uses the same array, which keeps the contents of
  *     the last call.  Nothing in it needs to start at zero (each partial
  *     result is written before it is read), but calls that overlap on the GPU
@@ -228,7 +230,7 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float
  * Other arguments, results and errors as attn_fwd_splitkv.
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
-int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+ATTN_API int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
                              int B, int H, int Sq, int Skv, int d, int causal, float scale,
                              int dtype, int n_splits, void *stream);
 
@@ -252,17 +254,21 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *
  * fp32 arithmetic; asynchronous on `stream`.  Outputs must not overlap the
  * inputs or each other (ATTN_ERR_INVALID_ARG).
  */
-int attn_merge(const float *o_parts, const float *lse_parts, int n_parts, int64_t rows, int d,
+ATTN_API int attn_merge(const float *o_parts, const float *lse_parts, int n_parts, int64_t rows, int d,
                void *o, float *lse, int out_dtype, void *stream);
 
 /*
  * attn_check_status -- synchronises `stream`, then reads and clears the
  * library's device status word on the current device.  Returns
- * ATTN_ERR_TIMEOUT if any tensor-core kernel since the last check gave up a
- * bounded wait (its output is then incomplete), ATTN_ERR_CUDA if the stream
- * reports an error, ATTN_OK otherwise.
+ * ATTN_ERR_BOUNDS if, in the bounds-checking build (libattn_checked.so,
+ * compiled with ATTN_BOUNDS_CHECK), a kernel since the last check computed
+ * a global-memory index or TMA coordinate outside its buffer (the access was
+ * skipped, so the output is incomplete); ATTN_ERR_TIMEOUT if any tensor-core
+ * kernel since the last check gave up a bounded wait (its output is then
+ * incomplete); ATTN_ERR_CUDA if the stream reports an error; ATTN_OK
+ * otherwise.  The normal build never sets ATTN_ERR_BOUNDS.
  */
-int attn_check_status(void *stream);
+ATTN_API int attn_check_status(void *stream);
 
 /*
  * attn_shutdown -- releases what the library created on the current device
@@ -278,23 +284,13 @@ int attn_check_status(void *stream);
  * handle failed; the state is forgotten either way.  Not on the source
  * pages: resource management of this library.
  */
-int attn_shutdown(void);
+ATTN_API int attn_shutdown(void);
 
 /* Human-readable text for an attn_status value (static storage). */
-const char *attn_strerror(int status);
+ATTN_API const char *attn_strerror(int status);
 
 /* ATTN_ABI_VERSION of the loaded library. */
-int attn_abi_version(void);
-
-/*
- * Test hook for the watchdog of the tensor-core kernel.  hook = 0 (default)
- * disables it; hook = 1 makes the next launches skip one internal
- * completion signal, so that a bounded wait expires, the kernel stops
- * cleanly and attn_check_status reports ATTN_ERR_TIMEOUT.  timeout_ns sets
- * the bounded-wait limit (0 keeps the current value; default 1e9 ns).
- * Process-wide; not thread-safe against concurrent attn_fwd calls.
- */
-int attn_test_set_hook(int hook, uint64_t timeout_ns);
+ATTN_API int attn_abi_version(void);
 
 #ifdef __cplusplus
 }

@@ -16,9 +16,12 @@ import os
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED_DEVICE", "ATTN_ERR_LAUNCH",
-    "ATTN_ERR_TIMEOUT", "ATTN_ERR_CUDA", "ATTN_ERR_SCRATCH_LIMIT", "NOALLOC_SCRATCH_BYTES",
+    "ATTN_ERR_TIMEOUT", "ATTN_ERR_CUDA", "ATTN_ERR_SCRATCH_LIMIT", "ATTN_ERR_BOUNDS",
+    "NOALLOC_SCRATCH_BYTES",
     "ATTN_F32", "ATTN_BF16", "ATTN_F16", "ATTN_BF16_OUT_F32", "ATTN_F16_OUT_F32",
     "AttnError", "library_path", "load_library", "exported_symbols",
+    "test_library_path", "load_test_library", "test_exported_symbols",
+    "checked_library_path", "load_checked_library",
     "attn_fwd", "attn_validate", "attn_fwd_f32_blocked", "attn_fwd_staged",
     "attn_check_status", "attn_strerror", "attn_abi_version", "attn_test_set_hook",
     "attn_splitkv_workspace_size", "attn_splitkv_plan", "attn_fwd_splitkv", "attn_merge",
@@ -33,6 +36,7 @@ ATTN_ERR_LAUNCH = 3
 ATTN_ERR_TIMEOUT = 4
 ATTN_ERR_CUDA = 5
 ATTN_ERR_SCRATCH_LIMIT = 6
+ATTN_ERR_BOUNDS = 7  # the bounds-checking build (libattn_checked.so) only
 NOALLOC_SCRATCH_BYTES = 8 << 20  # the fixed scratch of attn_fwd_splitkv_noalloc
 
 ATTN_F32 = 0
@@ -43,21 +47,22 @@ ATTN_F16_OUT_F32 = 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
+_test_lib = None
+_checked_lib = None
 
 # (name, restype, argtypes) of every symbol declared in include/attn.h
+# (libattn.so) and, in _TEST_SIGS, in include/attn_test.h (libattn_test.so only)
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _SIGS = [
     ("attn_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     ("attn_validate", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I]),
-    ("attn_fwd_f32_blocked", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     ("attn_fwd_staged", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                              _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     ("attn_check_status", _I, [_P]),
     ("attn_strerror", ctypes.c_char_p, [_I]),
     ("attn_abi_version", _I, []),
-    ("attn_test_set_hook", _I, [_I, ctypes.c_uint64]),
     ("attn_splitkv_workspace_size", _I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     ("attn_splitkv_plan", _I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I),
                                ctypes.POINTER(ctypes.c_size_t)]),
@@ -67,6 +72,10 @@ _SIGS = [
     ("attn_fwd_splitkv_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                       _P]),
     ("attn_shutdown", _I, []),
+]
+_TEST_SIGS = [
+    ("attn_fwd_f32_blocked", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    ("attn_test_set_hook", _I, [_I, ctypes.c_uint64]),
 ]
 
 
@@ -80,25 +89,61 @@ def library_path() -> str:
     return os.environ.get("ATTN_GB300_LIB", os.path.join(_HERE, "libattn.so"))
 
 
+def test_library_path() -> str:
+    return os.environ.get("ATTN_GB300_TEST_LIB", os.path.join(_HERE, "libattn_test.so"))
+
+
+def _open(path, sigs, what):
+    if not os.path.exists(path):
+        raise ImportError("%s not found at %s: build it with "
+                          "online_softmax_forward_gb300.build.build()" % (what, path))
+    lib = ctypes.CDLL(path)
+    for name, res, args in sigs:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
 def load_library():
     """Load libattn.so (built by ``build.build()``); raises if it is absent."""
     global _lib
     if _lib is None:
-        path = library_path()
-        if not os.path.exists(path):
-            raise ImportError("libattn.so not found at %s: build it with "
-                              "online_softmax_forward_gb300.build.build()" % path)
-        lib = ctypes.CDLL(path)
-        for name, res, args in _SIGS:
-            fn = getattr(lib, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = lib
+        _lib = _open(library_path(), _SIGS, "libattn.so")
     return _lib
+
+
+def load_test_library():
+    """Load libattn_test.so: the product's functions plus the test-only entry
+    points of include/attn_test.h.  It is a separate library with its own
+    state (status word, hook): call the functions of a test on it alone."""
+    global _test_lib
+    if _test_lib is None:
+        _test_lib = _open(test_library_path(), _SIGS + _TEST_SIGS, "libattn_test.so")
+    return _test_lib
+
+
+def checked_library_path() -> str:
+    return os.path.join(_HERE, "libattn_checked.so")
+
+
+def load_checked_library():
+    """Load libattn_checked.so: the test library built with ATTN_BOUNDS_CHECK,
+    whose kernels test every global index and TMA coordinate before using it
+    (attn_check_status then reports ATTN_ERR_BOUNDS).  A separate library
+    with its own state, like the test library."""
+    global _checked_lib
+    if _checked_lib is None:
+        _checked_lib = _open(checked_library_path(), _SIGS + _TEST_SIGS, "libattn_checked.so")
+    return _checked_lib
 
 
 def exported_symbols():
     return [s[0] for s in _SIGS]
+
+
+def test_exported_symbols():
+    return [s[0] for s in _TEST_SIGS]
 
 
 def _strerror_safe(status: int) -> str:
@@ -127,8 +172,10 @@ def attn_validate(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, dtype):
 
 def attn_fwd_f32_blocked(q, k, v, o, lse, B, H, Sq, Skv, d, causal, scale, block_q,
                          block_kv, stream):
-    return load_library().attn_fwd_f32_blocked(q, k, v, o, lse, B, H, Sq, Skv, d, int(causal),
-                                               float(scale), block_q, block_kv, stream)
+    """Test library only (include/attn_test.h)."""
+    return load_test_library().attn_fwd_f32_blocked(q, k, v, o, lse, B, H, Sq, Skv, d,
+                                                    int(causal), float(scale), block_q,
+                                                    block_kv, stream)
 
 
 def attn_fwd_staged(q_host, k_host, v_host, o_host, lse_host, dq, dk, dv, do_, dlse,
@@ -155,7 +202,9 @@ def attn_shutdown():
 
 
 def attn_test_set_hook(hook, timeout_ns=0):
-    return load_library().attn_test_set_hook(int(hook), int(timeout_ns))
+    """Test library only (include/attn_test.h): arms the hook of
+    libattn_test.so, which affects that library's attn_fwd alone."""
+    return load_test_library().attn_test_set_hook(int(hook), int(timeout_ns))
 
 
 def attn_splitkv_workspace_size(B, H, Sq, d, n_splits):
@@ -291,7 +340,8 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out_dty
 
 def attention_f32_blocked(q, k, v, block_q: int, block_kv: int, causal: bool = False,
                           scale: float | None = None, stream=None):
-    """fp32 path with explicit tile sizes (block-size invariance tests)."""
+    """fp32 path with explicit tile sizes (block-size invariance tests;
+    runs in the test library, include/attn_test.h)."""
     import torch
     B, H, Sq, Skv, d = _shapes(q, k, v)
     out = torch.empty((B, H, Sq, d), dtype=torch.float32, device=q.device)

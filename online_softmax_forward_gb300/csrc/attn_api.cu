@@ -9,6 +9,9 @@
 
 #include "attn.h"
 #include "attn_internal.h"
+#ifdef ATTN_TEST_EXPORTS
+#include "attn_test.h"  // the test library's build of this file
+#endif
 
 namespace attn {
 
@@ -72,6 +75,14 @@ int check_device() {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return ATTN_ERR_UNSUPPORTED_DEVICE;
     const bool ok = (major == 10 && minor == 3);
+    if (ok) {
+        // Looking the no-alloc scratch up loads its module (and reserves the
+        // array) on this device now, in the first call of any entry point,
+        // rather than inside a later attn_fwd_splitkv_noalloc.  A failure
+        // here is not this call's concern: that entry point reports it.
+        void *scratch = nullptr;
+        (void)noalloc_scratch_ptr(&scratch);
+    }
     if (dev >= 0 && dev < kMaxDevices) __atomic_store_n(&g_device_ok[dev], ok ? 1 : 2, __ATOMIC_RELEASE);
     return ok ? ATTN_OK : ATTN_ERR_UNSUPPORTED_DEVICE;
 }
@@ -283,6 +294,7 @@ const char *attn_strerror(int status) {
     case ATTN_ERR_TIMEOUT: return "a kernel gave up a bounded wait; its output is incomplete";
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_SCRATCH_LIMIT: return "the problem needs more scratch than the fixed device array of attn_fwd_splitkv_noalloc holds";
+    case ATTN_ERR_BOUNDS: return "bounds-checking build: a kernel computed an index outside its buffer (the access was skipped)";
     default: return "unknown status";
     }
 }
@@ -302,6 +314,7 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
     return fwd_impl(q, k, v, o, lse, p, (cudaStream_t)stream);
 }
 
+#ifdef ATTN_TEST_EXPORTS
 int attn_fwd_f32_blocked(const float *q, const float *k, const float *v,
                          float *o, float *lse, int B, int H, int Sq, int Skv,
                          int d, int causal, float scale, int block_q,
@@ -318,6 +331,7 @@ int attn_fwd_f32_blocked(const float *q, const float *k, const float *v,
     if (p.Skv == 0) return launch_empty_keys(o, lse, p, (cudaStream_t)stream);
     return launch_f32(q, k, v, o, lse, p, block_q, block_kv, (cudaStream_t)stream);
 }
+#endif  // ATTN_TEST_EXPORTS
 
 int attn_fwd_staged(const void *q_host, const void *k_host, const void *v_host,
                     void *o_host, float *lse_host, void *dq, void *dk, void *dv,
@@ -474,8 +488,9 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *
     if (n_splits < 1 || n_splits > kMaxSplits || Sq > kMaxSplitRows) return ATTN_ERR_INVALID_ARG;
     if (p.bh() == 0 || Sq == 0) return ATTN_OK;
     size_t need = 0;
-    if (!splitkv_bytes(p.bh(), Sq, d, n_splits, &need) || need > kNoAllocScratchBytes)
-        return ATTN_ERR_SCRATCH_LIMIT;
+    if (!splitkv_bytes(p.bh(), Sq, d, n_splits, &need)) return ATTN_ERR_INVALID_ARG;
+    // an empty key set needs no scratch (it only writes o = 0, lse = -inf)
+    if (Skv > 0 && need > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH_LIMIT;
     st = check_device();
     if (st != ATTN_OK) return st;
     if (Skv == 0) return launch_empty_keys(o, lse, p, (cudaStream_t)stream);
@@ -527,10 +542,12 @@ int attn_check_status(void *stream) {
         if (cudaMemcpy(dptr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
             return ATTN_ERR_CUDA;
     }
+    if (word & kStatusBounds) return ATTN_ERR_BOUNDS;
     if (word & kStatusTimeout) return ATTN_ERR_TIMEOUT;
     return ATTN_OK;
 }
 
+#ifdef ATTN_TEST_EXPORTS
 int attn_test_set_hook(int hook, uint64_t timeout_ns) {
     if (hook < 0 || hook > 1) return ATTN_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_mu);
@@ -538,5 +555,6 @@ int attn_test_set_hook(int hook, uint64_t timeout_ns) {
     if (timeout_ns) g_watchdog_ns = timeout_ns;
     return ATTN_OK;
 }
+#endif  // ATTN_TEST_EXPORTS
 
 }  // extern "C"

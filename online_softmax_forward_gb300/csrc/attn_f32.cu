@@ -65,13 +65,16 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // Copy `rows` rows of D floats from global (row-major, contiguous) into a
 // shared tile with row stride `ld` floats, 16 bytes per thread per step.
+// `avail` is the number of rows from src to the end of its [S, D] slice
+// (the extent the bounds-checking build tests each row against).
 template <int D>
 __device__ __forceinline__ void stage_rows(float *dst, int ld, const float *__restrict__ src,
-                                           int rows) {
+                                           int rows, int avail, int *status) {
     constexpr int V4 = D / 4;
     const int n = rows * V4;
     for (int t = threadIdx.x; t < n; t += blockDim.x) {
         const int r = t / V4, c = (t % V4) * 4;
+        if (!in_bounds(r < avail, status)) continue;
         const float4 x = __ldg(reinterpret_cast<const float4 *>(src + (size_t)r * D + c));
         *reinterpret_cast<float4 *>(dst + r * ld + c) = x;
     }
@@ -81,7 +84,8 @@ template <int D>
 __global__ void __launch_bounds__(kWarps * 32)
 attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
                 const float *__restrict__ v, float *__restrict__ o, float *__restrict__ lse,
-                int Sq, int Skv, int causal, float scale, int block_q, int block_kv, int nqb) {
+                int BH, int Sq, int Skv, int causal, float scale, int block_q, int block_kv,
+                int nqb, int *status) {
     extern __shared__ __align__(16) float sm[];
     constexpr int LD = D + kPad;
     constexpr int CPL = (D + 31) / 32;  // output columns per lane
@@ -101,12 +105,13 @@ attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
     const int rows = q_end - q_start;
     const int off = Skv - Sq;  // causal: key j visible to query i iff j <= i + off
     float *Pw = Ps + warp * block_kv;
+    if (!in_bounds(bh < BH, status)) return;  // the whole block: bh is block-uniform
 
     const float *qg = q + ((size_t)bh * Sq + q_start) * D;
     const float *kg = k + (size_t)bh * Skv * D;
     const float *vg = v + (size_t)bh * Skv * D;
 
-    stage_rows<D>(Qs, LD, qg, rows);
+    stage_rows<D>(Qs, LD, qg, rows, Sq - q_start, status);
     for (int t = threadIdx.x; t < rows * D; t += blockDim.x) As[t] = 0.f;
     for (int t = threadIdx.x; t < rows; t += blockDim.x) {
         Ms[t] = -INFINITY;
@@ -118,8 +123,8 @@ attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
     for (int kv_start = 0; kv_start < kv_stop; kv_start += block_kv) {
         const int kv_end = min(kv_start + block_kv, Skv);
         __syncthreads();  // previous tile fully consumed (and Q staged)
-        stage_rows<D>(Ks, LD, kg + (size_t)kv_start * D, kv_end - kv_start);
-        stage_rows<D>(Vs, D, vg + (size_t)kv_start * D, kv_end - kv_start);
+        stage_rows<D>(Ks, LD, kg + (size_t)kv_start * D, kv_end - kv_start, Skv - kv_start, status);
+        stage_rows<D>(Vs, D, vg + (size_t)kv_start * D, kv_end - kv_start, Skv - kv_start, status);
         __syncthreads();
 
         for (int r = warp; r < rows; r += kWarps) {
@@ -188,12 +193,13 @@ attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
         const float l = Ls[r];
         const float inv = l > 0.f ? 1.f / l : 0.f;
         float *orow = o + ((size_t)bh * Sq + i) * D;
+        const bool row_in = in_bounds(((size_t)bh * Sq + i + 1) * D <= (size_t)BH * Sq * D, status);
 #pragma unroll
         for (int u = 0; u < CPL; ++u) {
             const int c = lane + 32 * u;
-            if (c < D) orow[c] = As[r * D + c] * inv;
+            if (c < D && row_in) orow[c] = As[r * D + c] * inv;
         }
-        if (lse && lane == 0) lse[(size_t)bh * Sq + i] = l > 0.f ? Ms[r] + logf(l) : -INFINITY;
+        if (lse && lane == 0 && row_in) lse[(size_t)bh * Sq + i] = l > 0.f ? Ms[r] + logf(l) : -INFINITY;
     }
 }
 
@@ -254,11 +260,13 @@ __device__ __forceinline__ void wg_sync(int g) {
 // zero-filled.
 template <int D>
 __device__ __forceinline__ void stage_async(float *dst, int ld, const float *__restrict__ src,
-                                            int row0, int n, int valid, int tid, int nthr) {
+                                            int row0, int n, int valid, int tid, int nthr,
+                                            int *status) {
     constexpr int V4 = D / 4;
     for (int f = tid; f < n * V4; f += nthr) {
         const int r = f / V4, c = (f - r * V4) * 4;
-        const bool in = row0 + r < valid;
+        const bool in = row0 + r < valid &&
+                        in_bounds((size_t)(row0 + r) * D + c + 4 <= (size_t)valid * D, status);
         const float *s = in ? src + (size_t)(row0 + r) * D + c : src;
         cp_async16(smem_addr(dst + r * ld + c), s, in ? 16 : 0);
     }
@@ -274,8 +282,8 @@ template <int D, int KS, int NS>
 __global__ void __launch_bounds__(KS * kWG, 1)
 attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
                       const float *__restrict__ v, float *__restrict__ o,
-                      float *__restrict__ lse, int Sq, int Skv, int causal, float scale_log2,
-                      int nqb) {
+                      float *__restrict__ lse, int BH, int Sq, int Skv, int causal,
+                      float scale_log2, int nqb, int *status) {
     using C = TiledCfg<D, KS, NS>;
     constexpr int LD = C::kLd, W = C::kW, NC = C::kNC;
     extern __shared__ __align__(16) float sm[];
@@ -291,6 +299,7 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
     const int q0 = (blockIdx.x % nqb) * kTQ;
     const int q_end = min(q0 + kTQ, Sq);
     const int off = Skv - Sq;  // causal: key j visible to query i iff j <= i + off
+    if (!in_bounds(bh < BH, status)) return;  // the whole block: bh is block-uniform
     const float *qg = q + (size_t)bh * Sq * D;
     const float *kg = k + (size_t)bh * Skv * D;
     const float *vg = v + (size_t)bh * Skv * D;
@@ -323,10 +332,10 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
     // group, so the first S starts while V is still arriving; one CTA barrier:
     // from here on Q is read-only and each warpgroup syncs alone
     if (ntiles > 0) {
-        stage_async<D>(Qs, LD, qg, q0, kTQ, Sq, threadIdx.x, KS * kWG);
-        if (g < ntiles) stage_async<D>(Ks, LD, kg, g * kTK, kTK, Skv, tid, kWG);
+        stage_async<D>(Qs, LD, qg, q0, kTQ, Sq, threadIdx.x, KS * kWG, status);
+        if (g < ntiles) stage_async<D>(Ks, LD, kg, g * kTK, kTK, Skv, tid, kWG, status);
         cp_async_commit();
-        if (g < ntiles) stage_async<D>(Vs, D, vg, g * kTK, kTK, Skv, tid, kWG);
+        if (g < ntiles) stage_async<D>(Vs, D, vg, g * kTK, kTK, Skv, tid, kWG, status);
         cp_async_commit();
         cp_async_wait1();
     }
@@ -336,8 +345,8 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
         const bool more = jt + KS < ntiles;
         if constexpr (C::kNS == 2) {
             if (more) {  // the other stage was released at the end of the last tile
-                stage_async<D>(Ks + (st ^ 1) * kTK * LD, LD, kg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
-                stage_async<D>(Vs + (st ^ 1) * kTK * D, D, vg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+                stage_async<D>(Ks + (st ^ 1) * kTK * LD, LD, kg, kv0 + KS * kTK, kTK, Skv, tid, kWG, status);
+                stage_async<D>(Vs + (st ^ 1) * kTK * D, D, vg, kv0 + KS * kTK, kTK, Skv, tid, kWG, status);
             }
             cp_async_commit();
             cp_async_wait1();  // everything but the copies just issued has landed
@@ -379,7 +388,7 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
             cp_async_wait0();  // V of this tile, the only copy in flight
             wg_sync(g);        // K is free for the next tile and V is visible
             if (more) {
-                stage_async<D>(Ks, LD, kg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+                stage_async<D>(Ks, LD, kg, kv0 + KS * kTK, kTK, Skv, tid, kWG, status);
                 cp_async_commit();
             }
         }
@@ -461,7 +470,7 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
         wg_sync(g);  // this stage and P are free for the next tile
         if constexpr (C::kNS == 1) {
             if (more) {
-                stage_async<D>(Vs, D, vg, kv0 + KS * kTK, kTK, Skv, tid, kWG);
+                stage_async<D>(Vs, D, vg, kv0 + KS * kTK, kTK, Skv, tid, kWG, status);
                 cp_async_commit();
                 cp_async_wait1();  // the next K; the next V may still be arriving
                 wg_sync(g);
@@ -496,6 +505,10 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
         for (int i = g; i < 4; i += KS) {
             const int row = q0 + ty + 8 * i;
             if (row >= Sq) continue;
+            // the last element this thread stores (o; lse lies inside the same rows)
+            if (!in_bounds(((size_t)bh * Sq + row) * D + tx * W + 64 * (NC - 1) + W <=
+                               (size_t)BH * Sq * D, status))
+                continue;
             float mm = -INFINITY;
 #pragma unroll
             for (int h = 0; h < KS; ++h) mm = fmaxf(mm, sm[C::kOffK + h * C::kStageK + i * kWG + tid]);
@@ -538,6 +551,9 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
     for (int i = 0; i < 4; ++i) {
         const int row = q0 + ty + 8 * i;
         if (row >= Sq) continue;
+        if (!in_bounds(((size_t)bh * Sq + row) * D + tx * W + 64 * (NC - 1) + W <=
+                           (size_t)BH * Sq * D, status))
+            continue;
         const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
         float *orow = o + ((size_t)bh * Sq + row) * D + tx * W;
 #pragma unroll
@@ -565,8 +581,11 @@ int launch_tiled_ks(const float *q, const float *k, const float *v, float *o, fl
     if (!set_smem_limit_once(reinterpret_cast<const void *>(attn_f32_tiled_kernel<D, KS, NS>),
                              (int)smem))
         return ATTN_ERR_LAUNCH;
+    int *status = status_word_device_ptr();
+    if (!status) return ATTN_ERR_CUDA;
     attn_f32_tiled_kernel<D, KS, NS><<<(unsigned)grid, KS * kWG, smem, stream>>>(
-        q, k, v, o, lse, p.Sq, p.Skv, p.causal, p.scale * 1.4426950408889634f, nqb);
+        q, k, v, o, lse, (int)p.bh(), p.Sq, p.Skv, p.causal, p.scale * 1.4426950408889634f, nqb,
+        status);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
@@ -639,8 +658,10 @@ int launch_d(const float *q, const float *k, const float *v, float *o, float *ls
     const int nqb = (p.Sq + bq - 1) / bq;
     const int64_t grid = p.bh() * nqb;
     if (grid > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+    int *status = status_word_device_ptr();
+    if (!status) return ATTN_ERR_CUDA;
     attn_f32_kernel<D><<<(unsigned)grid, kWarps * 32, smem, stream>>>(
-        q, k, v, o, lse, p.Sq, p.Skv, p.causal, p.scale, bq, bkv, nqb);
+        q, k, v, o, lse, (int)p.bh(), p.Sq, p.Skv, p.causal, p.scale, bq, bkv, nqb, status);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 

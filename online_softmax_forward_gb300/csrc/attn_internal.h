@@ -10,6 +10,35 @@ namespace attn {
 
 // Bit set in the device status word when a bounded wait expired.
 constexpr int kStatusTimeout = 1;
+// Bit set by the bounds-checking build when an index check failed.
+constexpr int kStatusBounds = 2;
+
+// The bounds-checking build (compiled with ATTN_BOUNDS_CHECK; the library
+// libattn_checked.so) tests every global-memory index and every TMA
+// coordinate a kernel computes against the extent of its buffer before the
+// access.  A failed test ORs kStatusBounds into the status word and the
+// access is skipped (a TMA load that fails its test also stops the CTA the
+// way an expired wait does); nothing traps.  attn_check_status then reports
+// ATTN_ERR_BOUNDS.  In the normal build the tests compile to nothing.
+#ifdef ATTN_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+
+#ifdef __CUDACC__
+// true if `ok`; otherwise records the failure in *status and returns false,
+// so that the caller skips the access.  Always true in the normal build.
+__device__ __forceinline__ bool in_bounds(bool ok, int *status) {
+    if constexpr (kBoundsCheck) {
+        if (!ok) {
+            atomicOr(status, kStatusBounds);
+            return false;
+        }
+    }
+    return true;
+}
+#endif
 
 // Host-side view of one problem.
 struct Problem {

@@ -164,7 +164,7 @@ template <int D, typename T, int RB>
 __global__ void __launch_bounds__(SkvCfg<D, T>::kWarps * 32)
 splitkv_partial_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                        float *__restrict__ part_o, float *__restrict__ part_lse, int BH, int Sq,
-                       int Skv, int causal, float sl2, int chunk) {
+                       int Skv, int causal, float sl2, int chunk, int *status) {
     using C = SkvCfg<D, T>;
     using U = Unpack16<T>;
     constexpr int W = C::kWarps;
@@ -179,6 +179,9 @@ splitkv_partial_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
     // the merge kernel that follows may be scheduled now; it waits for this
     // grid to complete before it reads anything (griddepcontrol.wait)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the whole block (bh, split and row0 are block-uniform); the partial
+    // results it skips are then never written
+    if (!in_bounds(bh < BH && row0 < Sq, status)) return;
     const int off = Skv - Sq;  // causal: key j visible to query i iff j <= i + off
     const int kb = split * chunk;
     int ke = min(Skv, kb + chunk);
@@ -187,7 +190,9 @@ splitkv_partial_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
 
     for (int t = threadIdx.x; t < RB * D; t += blockDim.x) {
         const int i = t / D, c = t % D;
-        Qs[t] = i < nrows ? to_f32<T>(q[((size_t)bh * Sq + row0 + i) * D + c]) * sl2 : 0.f;
+        const size_t qi = ((size_t)bh * Sq + row0 + i) * D + c;
+        Qs[t] = i < nrows && in_bounds(qi < (size_t)BH * Sq * D, status)
+                    ? to_f32<T>(q[qi]) * sl2 : 0.f;
     }
     __syncthreads();
 
@@ -216,7 +221,8 @@ splitkv_partial_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
             const int g = it2 * 32 + lane;
             const int r = g / C::kChunks, c = g % C::kChunks;
             const int j = kb + tile * kTileKeys + r;
-            const bool in = j < ke;
+            const bool in = j < ke &&
+                            in_bounds((size_t)j * D + (c + 1) * C::kElems16 <= (size_t)Skv * D, status);
             const size_t src = (size_t)(in ? j : kb) * D + c * C::kElems16;
             const uint32_t dst = kbase + r * C::kRow + c * 16;
             cp_async16(dst, kg + src, in ? 16 : 0);
@@ -330,6 +336,8 @@ splitkv_partial_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
         }
     __syncthreads();
     const size_t prow = ((size_t)split * BH + bh) * Sq + row0;  // first row of this block
+    const size_t part_rows = (size_t)gridDim.y * BH * Sq;        // rows of the workspace used
+    if (!in_bounds(prow + nrows <= part_rows, status)) return;   // block-uniform
     for (int t = threadIdx.x; t < nrows * D; t += blockDim.x) {
         const int i = t / D, c = t % D;
         float M = -INFINITY;
@@ -381,13 +389,16 @@ __device__ __forceinline__ float block_reduce(float x, float *red, bool is_max) 
 template <typename TO>
 __global__ void __launch_bounds__(kMergeThreads)
 merge_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_parts,
-             int64_t rows, int d, TO *__restrict__ o, float *__restrict__ lse) {
+             int64_t rows, int d, TO *__restrict__ o, float *__restrict__ lse, int *status) {
     extern __shared__ float wts[];  // [n_parts]
     // launched as a programmatic dependent of the partial kernel: its results
     // are complete and visible after this wait (no-op without a predecessor)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float red[kMergeThreads / 32];
     const int64_t row = blockIdx.x;
+    // every index below is p * rows + row or (p * rows + row) * d + c with
+    // p < n_parts, c < d: inside the buffers once row < rows
+    if (!in_bounds(row < rows, status)) return;  // block-uniform
     TO *orow = o + row * d;
     float M = -INFINITY;
     for (int p = threadIdx.x; p < n_parts; p += kMergeThreads)
@@ -432,11 +443,15 @@ constexpr int kMergeRowWarps = 8;  // rows per CTA
 template <typename TO>
 __global__ void __launch_bounds__(kMergeRowWarps * 32)
 merge_rows_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_parts,
-                  int64_t rows, int d, TO *__restrict__ o, float *__restrict__ lse) {
+                  int64_t rows, int d, TO *__restrict__ o, float *__restrict__ lse,
+                  int *status) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * kMergeRowWarps + (threadIdx.x >> 5);
     if (row >= rows) return;  // the whole warp: one row per warp
+    // lane p < n_parts reads part p: the indices stay inside the buffers when
+    // the parts fit one lane each
+    if (!in_bounds(n_parts <= 32 && row >= 0, status)) return;
     const float lp = lane < n_parts ? pl[(int64_t)lane * rows + row] : -INFINITY;
     const float M = warp_max(lp);
     TO *orow = o + row * d;
@@ -488,11 +503,13 @@ int launch_merge_t(const float *po, const float *pl, int n_parts, int64_t rows, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    int *status = status_word_device_ptr();
+    if (!status) return ATTN_ERR_CUDA;
     const cudaError_t e =
         by_warp ? cudaLaunchKernelEx(&cfg, merge_rows_kernel<TO>, po, pl, n_parts, rows, d,
-                                     reinterpret_cast<TO *>(o), lse)
+                                     reinterpret_cast<TO *>(o), lse, status)
                 : cudaLaunchKernelEx(&cfg, merge_kernel<TO>, po, pl, n_parts, rows, d,
-                                     reinterpret_cast<TO *>(o), lse);
+                                     reinterpret_cast<TO *>(o), lse, status);
     return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
@@ -504,10 +521,12 @@ int launch_partial(const void *q, const void *k, const void *v, float *po, float
     auto kern = splitkv_partial_kernel<D, T, RB>;
     if (!set_smem_limit_once(reinterpret_cast<const void *>(kern), (int)smem)) return ATTN_ERR_LAUNCH;
     const dim3 grid((unsigned)p.bh(), (unsigned)n_eff, (unsigned)((p.Sq + RB - 1) / RB));
+    int *status = status_word_device_ptr();
+    if (!status) return ATTN_ERR_CUDA;
     kern<<<grid, SkvCfg<D, T>::kWarps * 32, smem, stream>>>(
         reinterpret_cast<const T *>(q), reinterpret_cast<const T *>(k),
         reinterpret_cast<const T *>(v), po, pl, (int)p.bh(), p.Sq, p.Skv, p.causal,
-        p.scale * 1.4426950408889634f, chunk);
+        p.scale * 1.4426950408889634f, chunk, status);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 

@@ -37,8 +37,13 @@
 //    32-column stores (no swizzle, no proxy fence; 7-9 % faster).  The running max is updated lazily: O and l are
 //    rescaled (O in TMEM, after the previous P.V has completed) only when the
 //    max grows by more than 2^8, so P stays <= 256; O, l and m always refer
-//    to the same stale max, so the result is the same softmax.  After the
-//    last tile they write O / l and lse = m + ln l.
+//    to the same stale max, so the result is the same softmax.  Each row
+//    keeps two normalisers: l, the sum of the exact P, gives the lse; lr
+//    adds to it, tile by tile, the rounding error of the tile's largest P in
+//    its 16-bit form -- the term a stale max makes large (up to 256 * 2^-9)
+//    -- so that O / lr divides by (almost exactly) the sum of the weights
+//    P.V multiplied.  After the last tile they write O / lr and
+//    lse = m + ln l.
 //  * Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0, O1 after;
 //    at d = 64 also P0 [384,448) and P1 [448,512), 16-bit pairs per column.
 //  * Every mbarrier wait is bounded (globaltimer).  On expiry the CTA sets an
@@ -298,7 +303,7 @@ __device__ __forceinline__ float max_half(const Half &h) {
 }
 
 // P = 2^(s * sl2 - mb) for 32 keys: packed 16-bit pairs into pk, fp32
-// partial sums into acc.
+// partial sums of the exact values into acc.
 template <bool kBF16>
 __device__ __forceinline__ void exp32(const uint32_t (&r)[32], float sl2, float mb,
                                       uint32_t *pk, float2 (&acc)[4]) {
@@ -310,6 +315,16 @@ __device__ __forceinline__ void exp32(const uint32_t (&r)[32], float sl2, float 
         acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
         pk[i] = pack2<kBF16>(p0, p1);
     }
+}
+
+// Rounding error of the largest probability of a tile, 2^(smax * sl2 - mb),
+// when it is stored as a 16-bit P: its 16-bit value minus its exact value.
+// The value is computed by the same instructions as in exp32, so it is the
+// same number P.V multiplies.
+template <bool kBF16>
+__device__ __forceinline__ float max_p_rounding(float smax, float sl2, float mb) {
+    const float p = ptx::ex2_approx(fmaf(smax, sl2, -mb));
+    return ptx::add_f32_half<kBF16, false>(0.f, pack2<kBF16>(p, p)) - p;
 }
 
 template <int D, bool kBF16>
@@ -386,9 +401,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             uint32_t qn[2] = {0, 0}, q_last_par[2] = {0, 0};
             bool q_loaded[2] = {false, false};
             bool ok = true;
+            // a TMA coordinate that fails the bounds-checking build's test stops
+            // the CTA the way an expired wait does
+            auto stop = [&]() {
+                *watch.abort_flag = 1;
+                return false;
+            };
             auto load_kv = [&](const CUtensorMap *tm, int j, int bh) {
                 const int s = pos % kStages;
                 if (!watch.wait(bar(bars->kv_empty[s]), ((pos / kStages) & 1) ^ 1)) return false;
+                if (!in_bounds(j >= 0 && j * BN < p.Skv && bh >= 0 && bh < p.BH, p.status))
+                    return stop();
                 ptx::mbar_arrive_expect_tx(bar(bars->kv_full[s]), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     ptx::tma_load_3d(sKV + s * C::kTileBytes + c * C::kChunkBytes, tm,
@@ -406,6 +429,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (w.nkv[t] == 0) continue;
                     if (!watch.wait(bar(bars->q_empty[t]), (qn[t] & 1) ^ 1)) { ok = false; break; }
+                    if (!in_bounds(w.q0 + t * BM < p.Sq && w.bh >= 0 && w.bh < p.BH, p.status)) {
+                        ok = stop();
+                        break;
+                    }
                     ptx::mbar_arrive_expect_tx(bar(bars->q_full[t]), C::kTileBytes);
                     for (int c = 0; c < C::kChunks; ++c)
                         ptx::tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
@@ -562,7 +589,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const int row = w.q0 + t * BM + r;  // query index of this thread
             const int limit = p.causal ? min(p.Skv, row + off + 1) : p.Skv;  // keys < limit visible
             float m = -INFINITY;  // running max, log2-scaled units
-            float l = 0.f;        // running normaliser relative to m
+            // running normalisers relative to m: l sums the exact P (for the
+            // lse); lr is l with each tile's largest P taken at its 16-bit
+            // value, the one P.V multiplies (for the output)
+            float l = 0.f;
+            float lr = 0.f;
 
             for (int j = 0; j < nk; ++j) {
                 const bool got = watch.wait(bar(bars->s_full[t]), sn & 1);
@@ -596,7 +627,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(bars->s_free[t]));
                 mask_half(rb, kv0 + 64, limit);
-                const float m_new = fmaxf(m, fmaxf(mxa, max_half(rb)) * sl2);
+                const float smax = fmaxf(mxa, max_half(rb));  // raw maximum of the tile
+                const float m_new = fmaxf(m, smax * sl2);
                 bool rescale = false;
                 float alpha = 1.f;
                 if (m == -INFINITY) {
@@ -606,6 +638,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     alpha = ptx::ex2_approx(m - m_new);
                     m = m_new;
                     l *= alpha;
+                    lr *= alpha;
                 }
                 // P_t(j-1) . V must be complete before O_t is rescaled or the P
                 // buffer is overwritten
@@ -671,7 +704,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(bars->p_full[t]));
                 const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
-                l += (s01.x + s01.y) + (s23.x + s23.y);
+                const float tile_sum = (s01.x + s01.y) + (s23.x + s23.y);
+                l += tile_sum;
+                lr += tile_sum + max_p_rounding<kBF16>(smax, sl2, mb);
             }
             if (!ok) break;
 
@@ -682,9 +717,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 ptx::tc_fence_after();
             }
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = lr > 0.f ? 1.f / lr : 0.f;
             const bool live = row < p.Sq;
             const size_t orow = ((size_t)w.bh * p.Sq + row) * D;
+            const size_t o_elems = (size_t)p.BH * p.Sq * D;  // extent of o (and lse / D)
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -699,6 +735,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 if (!live) {
                     // rows past Sq: nothing to store
+                } else if (!in_bounds(orow + (size_t)(c + 1) * 32 <= o_elems, p.status)) {
+                    // bounds-checking build: the store is skipped
                 } else if (p.out_f32) {
                     float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + orow + c * 32);
 #pragma unroll
@@ -720,7 +758,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                 }
             }
-            if (live && p.lse)
+            if (live && p.lse && in_bounds(orow < o_elems, p.status))
                 p.lse[(size_t)w.bh * p.Sq + row] =
                     l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             if (nk > 0) {

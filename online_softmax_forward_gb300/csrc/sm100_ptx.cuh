@@ -259,6 +259,30 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
+// c + (float)h, h the low (kHigh = false) or high half of the packed pair
+// `pk`, read as bf16 (kBF16) or fp16: the mixed-precision add of the sm_100
+// family, so a sum of 16-bit values needs no separate unpacking.
+template <bool kBF16, bool kHigh>
+__device__ __forceinline__ float add_f32_half(float c, uint32_t pk) {
+    float d;
+    if constexpr (kBF16) {
+        if constexpr (kHigh)
+            asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+                "add.rn.f32.bf16 %0, hi, %2;\n\t}" : "=f"(d) : "r"(pk), "f"(c));
+        else
+            asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+                "add.rn.f32.bf16 %0, lo, %2;\n\t}" : "=f"(d) : "r"(pk), "f"(c));
+    } else {
+        if constexpr (kHigh)
+            asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+                "add.rn.f32.f16 %0, hi, %2;\n\t}" : "=f"(d) : "r"(pk), "f"(c));
+        else
+            asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+                "add.rn.f32.f16 %0, lo, %2;\n\t}" : "=f"(d) : "r"(pk), "f"(c));
+    }
+    return d;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

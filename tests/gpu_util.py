@@ -41,7 +41,9 @@ def run(q, k, v, causal, dtype=torch.float32, out_dtype=None, scale=None, blocks
     else:
         o, lse = pkg.attention(qd, kd, vd, causal=causal, scale=scale, out_dtype=out_dtype)
     torch.cuda.synchronize()
-    st = pkg.attn_check_status(None)
+    # the blocked entry point runs in the test library, which has its own status word
+    lib = pkg.load_test_library() if blocks is not None else pkg.load_library()
+    st = lib.attn_check_status(None)
     assert st == pkg.ATTN_OK, pkg.attn_strerror(st)
     return o.double().cpu().numpy(), lse.double().cpu().numpy()
 

@@ -1,6 +1,7 @@
 """Host-only checks of the C ABI: the library loads without a GPU, exports
-every function include/attn.h declares, and rejects invalid arguments before
-any CUDA call (attn_validate never dereferences its pointers)."""
+every function include/attn.h declares (and the test library also those of
+include/attn_test.h), and rejects invalid arguments before any CUDA call
+(attn_validate never dereferences its pointers)."""
 import math
 import os
 import re
@@ -19,10 +20,11 @@ def lib():
     return pkg.load_library()
 
 
-def header_functions():
-    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+def header_functions(name="attn.h"):
+    text = open(os.path.join(ROOT, "include", name)).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:ATTN_API\s+)?(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(",
+                                 text, flags=re.M)))
 
 
 def defined_symbols(path):
@@ -42,9 +44,32 @@ def test_every_declared_function_is_exported(lib):
         assert hasattr(lib, name)
 
 
+def test_product_library_exports_nothing_else(lib):
+    """libattn.so exports the functions of attn.h and no other function of
+    its own: the test-only entry points are absent, and nothing internal
+    (C++ symbols of the attn namespace, kernels) is visible."""
+    syms = defined_symbols(pkg.library_path())
+    for name in header_functions("attn_test.h"):
+        assert name not in syms, name
+    ours = {s for s in syms if s.startswith("attn") or "4attn" in s}
+    assert ours == set(header_functions())
+
+
+def test_test_library_exports_both_headers(lib):
+    test_only = header_functions("attn_test.h")
+    assert sorted(pkg.test_exported_symbols()) == test_only
+    assert set(test_only) == {"attn_fwd_f32_blocked", "attn_test_set_hook"}
+    syms = defined_symbols(pkg.test_library_path())
+    for name in header_functions() + test_only:
+        assert name in syms, name
+    tl = pkg.load_test_library()
+    for name in test_only:
+        assert hasattr(tl, name)
+
+
 def test_abi_version_and_messages(lib):
     assert pkg.attn_abi_version() == 1
-    for s in range(6):
+    for s in range(8):
         assert pkg.attn_strerror(s)
     assert "unknown" in pkg.attn_strerror(99)
 
@@ -90,7 +115,7 @@ def test_empty_problems_are_valid(lib):
 
 
 def test_blocked_entry_rejects_bad_tiles(lib):
-    f = pkg.load_library().attn_fwd_f32_blocked
+    f = pkg.load_test_library().attn_fwd_f32_blocked
     for bq, bkv in ((0, 16), (16, 0), (129, 16), (16, 257), (128, 256)):
         assert f(Q, K, V, O, L, 1, 1, 64, 64, 128, 0, 0.0, bq, bkv, None) == \
             pkg.ATTN_ERR_INVALID_ARG
@@ -193,3 +218,14 @@ def test_torch_wrappers_reject_host_tensors_before_any_call(lib):
         pkg.attention_splitkv(q, q, q, n_splits=1)
     with pytest.raises(ValueError, match="CUDA"):
         pkg.merge(torch.zeros(2, 4, 64), torch.zeros(2, 4))
+
+
+def test_checked_library_exports_the_test_library_functions(lib):
+    """libattn_checked.so, the bounds-checking build, carries the same entry
+    points as the test library."""
+    syms = defined_symbols(pkg.checked_library_path())
+    for name in header_functions() + header_functions("attn_test.h"):
+        assert name in syms, name
+    cl = pkg.load_checked_library()
+    assert cl.attn_abi_version() == 1
+    assert cl.attn_strerror(pkg.ATTN_ERR_BOUNDS).decode().startswith("bounds-checking build")

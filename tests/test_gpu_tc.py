@@ -59,24 +59,20 @@ def test_small_shapes_16bit_out(case, dtype):
     assert_lse_close(lse, lse_ref, 1e-4)
 
 
-def test_large_scores_stay_finite():
-    """The large-score exercise (scores x 50, q multiplied by 50).  Rows are
-    then dominated by one or two keys, and each 16-bit probability carries a
-    relative rounding error of at most 2^-9 (bf16) -- including the dominant
-    one, whose value is 2^x for a stale running maximum.  The error bound
-    that follows from that arithmetic, |o - o_ref| <= 2 * 2^-9 * max|v|, is
-    asserted here; the mean and the lse keep the standard bounds."""
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_large_scores_stay_finite(dtype):
+    """The large-score exercise (scores x 50, q multiplied by 50): rows are
+    dominated by one or two keys, so the 16-bit rounding of the dominant
+    probability would show in full if the normaliser did not sum exactly the
+    rounded probabilities that multiply V.  The standard bounds hold: max abs
+    <= 1e-2, mean abs <= 1e-3, lse within 1e-4 * max(1, |lse|)."""
     q, k, v = qkv_inputs.normal_qkv(1, 2, 256, 512, 128, seed=9)
-    q = (q * 50).to(torch.bfloat16)
-    k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    q = (q * 50).to(dtype)
+    k, v = k.to(dtype), v.to(dtype)
     o_ref, lse_ref = oracle.attention(q, k, v, causal=False)
-    o, lse = run(q, k, v, False, dtype=torch.bfloat16, out_dtype=torch.float32)
+    o, lse = run(q, k, v, False, dtype=dtype, out_dtype=torch.float32)
     assert np.all(np.isfinite(o))
-    err = np.abs(o - o_ref)
-    bound = 2.0 * 2.0 ** -9 * float(v.float().abs().max())
-    assert err.max() <= bound, (err.max(), bound)
-    assert err.mean() <= 1e-3
-    assert_lse_close(lse, lse_ref, 1e-4)
+    assert_bf16_parity(o, lse, o_ref, lse_ref)
 
 
 def test_rising_maximum_forces_rescale():

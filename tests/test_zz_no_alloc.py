@@ -72,3 +72,71 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
                                       Sq, 64, d, 0, 0.0, pkg.ATTN_BF16, n, None)
     assert st == pkg.ATTN_ERR_SCRATCH_LIMIT
     assert "scratch" in pkg.attn_strerror(st)
+
+
+def test_noalloc_size_errors_on_the_host():
+    """Host-side checks before any launch (fake, never touched addresses, far
+    enough apart that no two arguments overlap): a problem with no keys needs
+    no scratch, so its size never meets the scratch limit; a problem whose
+    scratch size does not fit in 64 bits is an invalid argument, as it is
+    for attn_fwd_splitkv."""
+    ensure_built()
+    gib4 = 1 << 32
+    B, H, Sq, d, n = 64, 64, 8, 128, 4  # more than the scratch holds, had it keys
+    if torch.cuda.is_available():
+        # with a device the call goes on to write o = 0, lse = -inf: real buffers
+        o = torch.full((B, H, Sq, d), 7.0, dtype=torch.bfloat16, device="cuda")
+        lse = torch.zeros((B, H, Sq), dtype=torch.float32, device="cuda")
+        q = torch.zeros_like(o)
+        st = pkg.attn_fwd_splitkv_noalloc(q.data_ptr(), None, None, o.data_ptr(),
+                                          lse.data_ptr(), B, H, Sq, 0, d, 0, 0.0,
+                                          pkg.ATTN_BF16, n, None)
+        torch.cuda.synchronize()
+        assert st == pkg.ATTN_OK
+        assert bool((o == 0).all()) and bool(torch.isneginf(lse).all())
+    else:
+        # without one the device check refuses it, after the size checks
+        st = pkg.attn_fwd_splitkv_noalloc(1 * gib4, 2 * gib4, 3 * gib4, 4 * gib4, 5 * gib4,
+                                          B, H, Sq, 0, d, 0, 0.0, pkg.ATTN_BF16, n, None)
+        assert st == pkg.ATTN_ERR_UNSUPPORTED_DEVICE
+    big = 1 << 60
+    B = H = 46340  # B * H just below 2^31; 256 splits of 524280 rows overflow
+    st = pkg.attn_fwd_splitkv_noalloc(1 * big, 2 * big, 3 * big, 4 * big, 5 * big, B, H,
+                                      524280, 64, 128, 0, 0.0, pkg.ATTN_BF16, 256, None)
+    assert st == pkg.ATTN_ERR_INVALID_ARG
+    st = pkg.attn_fwd_splitkv(1 * big, 2 * big, 3 * big, 4 * big, 5 * big, B, H, 524280, 64,
+                              128, 0, 0.0, pkg.ATTN_BF16, 256, 6 * big, 1 << 40, None)
+    assert st == pkg.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.gpu
+def test_noalloc_later_calls_leave_free_memory_unchanged():
+    """Once a call of the same kind has run on the device (which loads the
+    library's device code there, the scratch array included), further calls
+    take nothing from the device's free memory, and give the same bits."""
+    ensure_built()
+    B, H, Sq, Skv, d = 2, 8, 3, 5000, 128
+    q, k, v = (t.to(torch.bfloat16).cuda()
+               for t in qkv_inputs.normal_qkv(B, H, Sq, Skv, d, seed=40))
+    st, n_splits, _ = pkg.attn_splitkv_plan(B, H, Sq, Skv, d, pkg.ATTN_BF16)
+    assert st == pkg.ATTN_OK
+    outs = [(torch.empty((B, H, Sq, d), dtype=torch.bfloat16, device="cuda"),
+             torch.empty((B, H, Sq), dtype=torch.float32, device="cuda")) for _ in range(3)]
+
+    def call(o, lse):
+        st = pkg.attn_fwd_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                          o.data_ptr(), lse.data_ptr(), B, H, Sq, Skv, d, 0,
+                                          0.0, pkg.ATTN_BF16, n_splits, None)
+        assert st == pkg.ATTN_OK, pkg.attn_strerror(st)
+
+    call(*outs[0])  # set-up call
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    call(*outs[1])
+    call(*outs[2])
+    torch.cuda.synchronize()
+    free_after = torch.cuda.mem_get_info()[0]
+    assert free_after == free_before
+    assert pkg.attn_check_status(None) == pkg.ATTN_OK
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
