@@ -104,6 +104,13 @@ typedef enum attn_dtype {
  * only enqueues one kernel on `stream` (two for attn_fwd_splitkv) and may be
  * captured into a CUDA graph; a replay reads whatever the captured pointers
  * hold at replay time.  Make one ordinary call of the shape before capturing.
+ *
+ * Work distribution (16-bit types): each launch of the tensor-core kernel
+ * takes its work units from one of 256 device counters of the library,
+ * chosen in turn, and returns that counter to zero when it ends.  At most
+ * 256 such launches may therefore be in flight on one device at once, and a
+ * CUDA graph containing the call must not be replayed concurrently with
+ * itself (its replays share the counter captured with it).
  */
 ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              int B, int H, int Sq, int Skv, int d, int causal, float scale,

@@ -282,6 +282,7 @@ int attn_shutdown(void) {
         g_smem_n = n;
     }
     forget_noalloc_scratch(dev);
+    forget_sched_counters(dev);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -63,6 +63,7 @@ int launch_f32_tiled(const float *q, const float *k, const float *v, float *o,
 // 16-bit tensor-core path (attn_tc.cu).
 int launch_tc(const void *q, const void *k, const void *v, void *o, float *lse,
               const Problem &p, cudaStream_t stream);
+void forget_sched_counters(int dev);  // attn_shutdown: look the address up again next time
 
 // Split-KV path for few query rows (attn_splitkv.cu).
 constexpr int kSplitRowBlock = 8;  // query rows per split-KV CTA when Sq > 1

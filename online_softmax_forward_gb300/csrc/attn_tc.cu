@@ -10,8 +10,14 @@
 //
 //  * Persistent grid, one CTA per SM, 12 warps.  A work unit is two
 //    consecutive 128-row query tiles (Q0, Q1) of one (batch, head) slice; they
-//    share every K/V tile.  Units are handed out longest-first (causal) in a
-//    snake order.
+//    share every K/V tile.  Units are handed out dynamically: the producer
+//    of a CTA claims the next unit index from a device counter when it has
+//    issued the loads of the current one, and passes it to the CTA's other
+//    roles through a small ring in shared memory.  The order of the indices
+//    (decode_unit) takes the (batch, head) slices in groups of about one
+//    round of units, longest first inside a group, so the CTAs running at
+//    any time share the K and V of a few heads through L2: each K/V tile is
+//    read from HBM about once.
 //  * Warp 8 (producer) streams Q0/Q1 and the K/V tiles with TMA (128-byte
 //    swizzle) into a ring of shared-memory stages guarded by mbarriers, in
 //    the order the tensor core consumes them: K_0, then K_{j+1}, V_j for each
@@ -73,6 +79,14 @@ constexpr int kMmaWarp0 = 9;  // issuer of query tile 0; kMmaWarp0 + 1 issues ti
 constexpr int kThreads = 12 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units)
+// Work units are claimed from a device counter by the producer and passed to
+// the other roles through a ring of kSchedRing shared-memory slots; every warp
+// that reads a slot (issuers, softmax) releases it.
+constexpr int kSchedRing = 4;
+constexpr int kSchedReaders = 10;
+// Device counters of the dynamic schedule: kSchedSlots pairs (next unit,
+// CTAs done); each launch takes the next pair, and its last CTA resets it.
+constexpr int kSchedSlots = 256;
 // Register split: the block is launched with kLaunchRegs per thread; the two
 // softmax warpgroups grow to kSoftmaxRegs and the third warpgroup (producer,
 // issuers) shrinks to kOtherRegs.  The totals must match exactly.
@@ -96,7 +110,7 @@ struct Cfg {
     static constexpr int kOffP = 2 * kTileBytes;      // P0, P1 (shared memory at d = 128)
     static constexpr int kOffKV = kOffP + (kTmemP ? 0 : 2 * kPBytes);  // ring stages
     static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-    static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+    static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // + barriers + alignment slack
     // tensor-memory columns of S_t and O_t
     __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
     __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? (uint32_t)D : 0u); }
@@ -113,15 +127,18 @@ struct Bars {
     uint64_t p_free[2];   // P_t . V done: P buffer free, O_t up to date (MMA commit)
     uint64_t o_empty[2];  // epilogue has read O_t (128 arrivals)
     uint64_t mma_done[2];
+    uint64_t sched_full[kSchedRing], sched_empty[kSchedRing];
+    int sched_unit[kSchedRing];  // unit index, or -2: no more units
     uint32_t tmem_base;
     int abort_flag;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 struct TcParams {
     void *o;
     float *lse;
     int *status;
+    unsigned int *sched;  // this launch's counter pair: next unit, CTAs done
     int BH, Sq, Skv, causal;
     int nqb;      // units per (batch, head): ceil(Sq / 256)
     int hg;       // (batch, head) slices per schedule group (K/V of a group fit in L2)
@@ -138,8 +155,8 @@ struct Unit {
 };
 
 // Unit u of the schedule.  The (batch, head) slices are taken in groups of
-// hg whose K and V fit in L2 together; inside a group the units go level by
-// level, longest first for causal, and round-robin over the group's heads,
+// hg (about one unit per CTA in a group); inside a group the units go level
+// by level, longest first for causal, and round-robin over the group's heads,
 // so the CTAs running at any time share the K/V of a few heads through L2.
 __device__ __forceinline__ Unit decode_unit(int u, const TcParams &p) {
     Unit r;
@@ -164,17 +181,6 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcParams &p) {
         r.nkv[t] = n;
     }
     return r;
-}
-
-// Snake-ordered static schedule: round r hands unit r*G + c (even r) or
-// r*G + G-1-c (odd r) to CTA c.  Returns -2 when the rounds are exhausted and
-// -1 for an empty slot of the last round.
-__device__ __forceinline__ int unit_of(int round, const TcParams &p) {
-    const int G = gridDim.x, c = blockIdx.x;
-    const long base = (long)round * G;
-    if (base >= p.n_units) return -2;
-    const long u = base + ((round & 1) ? (G - 1 - c) : c);
-    return u < p.n_units ? (int)u : -1;
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.
@@ -362,6 +368,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ptx::mbar_init(bar(bars->o_empty[t]), 128);
             ptx::mbar_init(bar(bars->mma_done[t]), 1);
         }
+        for (int s = 0; s < kSchedRing; ++s) {
+            ptx::mbar_init(bar(bars->sched_full[s]), 1);
+            ptx::mbar_init(bar(bars->sched_empty[s]), kSchedReaders);
+        }
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(bar(bars->kv_full[s]), 1);
             ptx::mbar_init(bar(bars->kv_empty[s]), 2);  // one arrival per issuer
@@ -389,6 +399,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto pos_k = [](uint32_t base, int j) { return base + (j == 0 ? 0u : (uint32_t)(2 * j - 1)); };
     auto pos_v = [](uint32_t base, int j, int n) {
         return base + (j + 1 < n ? (uint32_t)(2 * j + 2) : (uint32_t)(2 * j + 1));
+    };
+
+    // The next work unit for a consumer warp (issuer, softmax): the
+    // producer's k-th claim, read from ring slot k mod kSchedRing and released
+    // by one arrival per warp.  False if the CTA is aborting.
+    auto next_unit = [&](uint32_t &k, int &u) {
+        const uint32_t s = k % kSchedRing;
+        if (!__all_sync(0xffffffffu, watch.wait(bar(bars->sched_full[s]), (k / kSchedRing) & 1)))
+            return false;
+        u = *reinterpret_cast<volatile int *>(&bars->sched_unit[s]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(bars->sched_empty[s]));
+        ++k;
+        return true;
     };
 
     // Each role changes its register budget at the top of its own branch, so
@@ -419,13 +443,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ++pos;
                 return true;
             };
-            for (int round = 0; ok; ++round) {
-                const int u = unit_of(round, p);
-                if (u == -2) break;
-                if (u < 0) continue;
+            // Dynamic schedule: the next unit is claimed from the launch's counter
+            // once this unit's last load is issued (the claim's latency hides
+            // behind the ring), and published to the other roles.
+            unsigned claim = atomicAdd(p.sched, 1u);
+            for (uint32_t k = 0; ok; ++k) {
+                const uint32_t slot = k % kSchedRing;
+                if (!watch.wait(bar(bars->sched_empty[slot]), ((k / kSchedRing) & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                const int u = claim < (unsigned)p.n_units ? (int)claim : -2;
+                *reinterpret_cast<volatile int *>(&bars->sched_unit[slot]) = u;
+                ptx::mbar_arrive(bar(bars->sched_full[slot]));
+                if (u < 0) break;
                 const Unit w = decode_unit(u, p);
                 const int nmax = max(w.nkv[0], w.nkv[1]);
-                if (nmax == 0) continue;
+                if (nmax == 0) {
+                    claim = atomicAdd(p.sched, 1u);
+                    continue;
+                }
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (w.nkv[t] == 0) continue;
                     if (!watch.wait(bar(bars->q_empty[t]), (qn[t] & 1) ^ 1)) { ok = false; break; }
@@ -444,6 +481,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ok = ok && load_kv(&tm_k, 0, w.bh);
                 for (int j = 0; j < nmax && ok; ++j)
                     ok = (j + 1 >= nmax || load_kv(&tm_k, j + 1, w.bh)) && load_kv(&tm_v, j, w.bh);
+                if (ok) claim = atomicAdd(p.sched, 1u);
             }
             // teardown: wait until every load this thread issued has landed
             for (uint32_t s = 0; s < (uint32_t)kStages && s < pos; ++s) {
@@ -539,10 +577,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ptx::mma_commit_warp(bar(bars->kv_empty[st]));
             return true;
         };
-        for (int round = 0; ok; ++round) {
-            const int u = unit_of(round, p);
-            if (u == -2) break;
-            if (u < 0) continue;
+        for (uint32_t k = 0; ok;) {
+            int u;
+            if (!next_unit(k, u)) { ok = false; break; }
+            if (u < 0) break;
             const Unit w = decode_unit(u, p);
             const int nmax = max(w.nkv[0], w.nkv[1]);
             const int my = w.nkv[t];
@@ -580,10 +618,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         uint32_t sn = 0, pfn = 0;
         bool ok = true;
 
-        for (int round = 0; ok; ++round) {
-            const int u = unit_of(round, p);
-            if (u == -2) break;
-            if (u < 0) continue;
+        for (uint32_t k = 0; ok;) {
+            int u;
+            if (!next_unit(k, u)) { ok = false; break; }
+            if (u < 0) break;
             const Unit w = decode_unit(u, p);
             const int nk = w.nkv[t];
             const int row = w.q0 + t * BM + r;  // query index of this thread
@@ -777,9 +815,39 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();
     ptx::tc_fence_after();
     if (warp == kMmaWarp0) ptx::tmem_dealloc(tmem, kTmemCols);
+    // every CTA has made its last claim: the last one to finish resets the
+    // counter pair for a later launch
+    if (threadIdx.x == 0 && atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+        atomicExch(p.sched, 0u);
+        atomicExch(p.sched + 1, 0u);
+    }
 }
 
+// Counter pairs of the dynamic schedule (zero at module load; each launch
+// leaves its pair at zero again).
+__device__ unsigned int g_sched[kSchedSlots * 2];
+
 // ------------------------------------------------------------------ host side
+std::mutex g_sched_mu;
+unsigned int *g_sched_addr[64];
+std::atomic<unsigned> g_sched_seq{0};
+
+// The counter pair of the next launch on the current device; nullptr on error.
+unsigned int *next_sched_pair() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    unsigned int *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_sched_mu);
+        if (!g_sched_addr[dev]) {
+            void *a = nullptr;
+            if (cudaGetSymbolAddress(&a, g_sched) != cudaSuccess) return nullptr;
+            g_sched_addr[dev] = static_cast<unsigned int *>(a);
+        }
+        base = g_sched_addr[dev];
+    }
+    return base + 2 * (g_sched_seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+}
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -820,23 +888,29 @@ int launch_typed(const void *q, const void *k, const void *v, void *o, float *ls
         !make_map(&tv, v, kBF16, D, pr.Skv, BH))
         return ATTN_ERR_CUDA;
     int *status = status_word_device_ptr();
-    if (!status) return ATTN_ERR_CUDA;
+    unsigned int *sched = next_sched_pair();
+    if (!status || !sched) return ATTN_ERR_CUDA;
     TcParams p;
     p.o = o;
     p.lse = lse;
     p.status = status;
+    p.sched = sched;
     p.BH = (int)BH;
     p.Sq = pr.Sq;
     p.Skv = pr.Skv;
     p.causal = pr.causal;
     p.nqb = (pr.Sq + 2 * BM - 1) / (2 * BM);
+    const int sms = device_sm_count();
+    if (sms <= 0) return ATTN_ERR_CUDA;
     {
-        // heads per schedule group: all heads when their K and V fit in L2
-        // (about 160 MB with headroom); otherwise groups of about 64 MB
-        const int64_t kv_head = 2LL * pr.Skv * D * 2;
-        int64_t hg = BH;
-        if (kv_head > 0 && BH * kv_head > (160LL << 20)) hg = (int64_t)(64LL << 20) / kv_head;
+        // heads per schedule group: about one round of units (one per CTA), so
+        // that the CTAs running at any time work on the K and V of a few heads,
+        // which stay in L2 between the units that read them
+        // (the smallest divisor of B*H that covers a round: equal groups, so
+        // that no short group is left for the end, where it would run alone)
+        int64_t hg = ((int64_t)sms + p.nqb - 1) / p.nqb;
         if (hg < 1) hg = 1;
+        while (hg < BH && BH % hg != 0) ++hg;
         if (hg > BH) hg = BH;
         p.hg = (int)hg;
     }
@@ -847,8 +921,6 @@ int launch_typed(const void *q, const void *k, const void *v, void *o, float *ls
     p.out_f32 = (pr.dtype == ATTN_BF16_OUT_F32 || pr.dtype == ATTN_F16_OUT_F32) ? 1 : 0;
     p.hook = test_hook();
     p.timeout_ns = watchdog_ns();
-    const int sms = device_sm_count();
-    if (sms <= 0) return ATTN_ERR_CUDA;
     const int grid = (int)(n_units < sms ? n_units : sms);
     auto kern = attn_tc_kernel<D, kBF16>;
     // The register split inside the kernel (setmaxnreg) needs exactly the pool
@@ -873,6 +945,12 @@ int launch_typed(const void *q, const void *k, const void *v, void *o, float *ls
 }
 
 }  // namespace
+
+void forget_sched_counters(int dev) {
+    if (dev < 0 || dev >= 64) return;
+    std::lock_guard<std::mutex> lk(g_sched_mu);
+    g_sched_addr[dev] = nullptr;
+}
 
 int launch_tc(const void *q, const void *k, const void *v, void *o, float *lse,
               const Problem &p, cudaStream_t stream) {
