@@ -93,9 +93,10 @@ def test_rising_maximum_forces_rescale():
         assert_bf16_parity(o, lse, o_ref, lse_ref)
 
 
-def _sampled_parity(B, H, S, d, seed, n_random, heads=None, rows_per_head=None, causal=True):
+def _sampled_parity(B, H, S, d, seed, n_random, heads=None, rows_per_head=None, causal=True,
+                    dtype=torch.bfloat16):
     ensure_built()
-    q, k, v = qkv_inputs.normal_qkv(B, H, S, S, d, seed=seed, dtype=torch.bfloat16)
+    q, k, v = qkv_inputs.normal_qkv(B, H, S, S, d, seed=seed, dtype=dtype)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o32, lse = pkg.attention(qd, kd, vd, causal=causal, out_dtype=torch.float32)
     o16, lse16 = pkg.attention(qd, kd, vd, causal=causal)
@@ -131,7 +132,7 @@ def _sampled_parity(B, H, S, d, seed, n_random, heads=None, rows_per_head=None, 
     got = o32h[idx[:, 0], idx[:, 1]]
     got_l = lseh[idx[:, 0], idx[:, 1]]
     mx, mean = assert_bf16_parity(got, got_l, o_ref, lse_ref)
-    assert_rounded_output(o16h[idx[:, 0], idx[:, 1]], o_ref, torch.bfloat16)
+    assert_rounded_output(o16h[idx[:, 0], idx[:, 1]], o_ref, dtype)
     return mx, mean, len(rows)
 
 
@@ -141,6 +142,24 @@ def test_b1_h32_s8192_d128_causal_sampled():
     head (all tile boundaries) against the oracle."""
     mx, mean, n = _sampled_parity(1, 32, 8192, 128, seed=0, n_random=64)
     print("c4 sampled rows %d: max %.3e mean %.3e" % (n, mx, mean))
+
+
+def test_b1_h32_s8192_d128_fp16_causal_sampled():
+    """The same workload in fp16 (fp16 P for P.V, the other instruction
+    descriptor): every row checked for the properties; stratified rows of
+    eight heads against the oracle."""
+    mx, mean, n = _sampled_parity(1, 32, 8192, 128, seed=3, n_random=32,
+                                  heads=(0, 5, 10, 15, 16, 21, 26, 31), dtype=torch.float16)
+    print("fp16 8k sampled rows %d: max %.3e mean %.3e" % (n, mx, mean))
+
+
+def test_b1_h64_s8192_d64_causal_sampled():
+    """d = 64 at full size (P in tensor memory, six-stage ring; 64 heads, so
+    head groups of 8): every row checked for the properties; stratified rows
+    of eight heads against the oracle."""
+    mx, mean, n = _sampled_parity(1, 64, 8192, 64, seed=4, n_random=32,
+                                  heads=(0, 7, 8, 23, 40, 47, 56, 63))
+    print("d=64 8k sampled rows %d: max %.3e mean %.3e" % (n, mx, mean))
 
 
 def test_b1_h64_s32768_d128_causal_sampled():
