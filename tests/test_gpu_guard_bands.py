@@ -13,7 +13,8 @@ import torch
 import online_softmax_forward_gb300 as pkg
 import oracle
 import qkv_inputs
-from gpu_util import ensure_built
+from gpu_util import (assert_bf16_parity, assert_f32_parity, assert_rounded_output,
+                      ensure_built)
 
 pytestmark = pytest.mark.gpu
 
@@ -50,10 +51,15 @@ def test_attn_fwd_writes_only_its_outputs(case):
     check_guards(obuf, o.numel())
     check_guards(lbuf, lse.numel())
     o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=causal)
-    tol = 1e-5 if idt == torch.float32 else 2e-2
-    assert np.abs(o.double().cpu().numpy() - o_ref).max() <= tol
-    fin = np.isfinite(lse_ref)
-    assert np.array_equal(np.isfinite(lse.cpu().numpy()), fin)
+    on, ln = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    if idt == torch.float32:
+        assert_f32_parity(on, ln, o_ref, lse_ref)
+    elif odt == torch.float32:
+        assert_bf16_parity(on, ln, o_ref, lse_ref)
+    else:
+        assert_rounded_output(on, o_ref, odt)
+        fin = np.isfinite(lse_ref)
+        assert np.array_equal(np.isfinite(ln), fin)
 
 
 @pytest.mark.parametrize("case", [
