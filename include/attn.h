@@ -282,8 +282,8 @@ ATTN_API int attn_check_status(void *stream);
  * and forgets what it cached about it.  It destroys the two streams and three
  * events of attn_fwd_staged, after waiting for those streams to finish.  It
  * clears the cached capability check, SM count and kernel shared-memory
- * limits, and the device addresses of the status word and of the no-alloc
- * scratch.  Work the caller queued on its own streams is not waited for.
+ * limits, and the device addresses of the status word, of the no-alloc
+ * scratch and of the tensor-core kernel's schedule counters.  Work the caller queued on its own streams is not waited for.
  * The next call on the device sets everything up again.  Call it before
  * cudaDeviceReset if the process goes on using the library, since a reset
  * invalidates those handles.  It must not run concurrently with other calls
