@@ -74,3 +74,47 @@ def test_aborted_launch_returns_its_counter():
     assert tl.attn_check_status(None) == pkg.ATTN_OK
     for o, lse in outs:
         assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)
+
+
+def test_concurrent_host_threads():
+    """Four host threads call the library at the same time, each on its own
+    stream and with its own outputs (the calls release the interpreter lock):
+    the per-device caches, the choice of counter pairs and the kernels running
+    side by side must not disturb one another."""
+    import threading
+    ensure_built()
+    q, k, v = _problem()
+    ref_o, ref_l = pkg.attention(q, k, v, causal=True)
+    qf, kf, vf = (t.float() for t in (q[:, :1, :200, :64], k[:, :1, :200, :64], v[:, :1, :200, :64]))
+    qf, kf, vf = (t.contiguous() for t in (qf, kf, vf))
+    ref_f, _ = pkg.attention(qf, kf, vf, causal=True)
+    torch.cuda.synchronize()
+    n_threads, n_calls = 4, 40
+    outs = [[(torch.full_like(ref_o, float("nan")), torch.full_like(ref_l, float("nan")),
+              torch.full_like(ref_f, float("nan"))) for _ in range(n_calls)]
+            for _ in range(n_threads)]
+    streams = [torch.cuda.Stream() for _ in range(n_threads)]
+    errors = []
+
+    def work(i):
+        try:
+            torch.cuda.set_device(q.device)
+            for o, lse, of in outs[i]:
+                pkg.attention(q, k, v, causal=True, out=o, lse=lse, stream=streams[i])
+                pkg.attention(qf, kf, vf, causal=True, out=of, return_lse=False,
+                              stream=streams[i])
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(n_threads)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for s in streams:
+        assert pkg.attn_check_status(s.cuda_stream) == pkg.ATTN_OK
+    for i in range(n_threads):
+        for o, lse, of in outs[i]:
+            assert torch.equal(o, ref_o) and torch.equal(lse, ref_l) and torch.equal(of, ref_f)
