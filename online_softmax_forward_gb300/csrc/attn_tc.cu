@@ -907,10 +907,16 @@ int launch_typed(const void *q, const void *k, const void *v, void *o, float *ls
         // that the CTAs running at any time work on the K and V of a few heads,
         // which stay in L2 between the units that read them
         // (the smallest divisor of B*H that covers a round: equal groups, so
-        // that no short group is left for the end, where it would run alone)
-        int64_t hg = ((int64_t)sms + p.nqb - 1) / p.nqb;
-        if (hg < 1) hg = 1;
+        // that no short group is left for the end, where it would run alone).
+        // Without such a divisor all heads form one group -- unless their K and
+        // V exceed what L2 holds, where round-sized groups with a smaller last
+        // one cost less than reading K and V from HBM once per round of units.
+        int64_t h0 = ((int64_t)sms + p.nqb - 1) / p.nqb;
+        if (h0 < 1) h0 = 1;
+        int64_t hg = h0;
         while (hg < BH && BH % hg != 0) ++hg;
+        const int64_t kv_bytes = BH * 2LL * pr.Skv * D * 2;
+        if (hg >= BH && kv_bytes > (96LL << 20)) hg = h0;
         if (hg > BH) hg = BH;
         p.hg = (int)hg;
     }

@@ -181,6 +181,16 @@ def test_grouped_schedule_noncausal_sampled():
     print("grouped non-causal sampled rows %d: max %.3e mean %.3e" % (n, mx, mean))
 
 
+def test_unequal_head_groups_sampled():
+    """B=1, H=7, Sq=Skv=32768, d=128, non-causal: 7 heads have no divisor
+    covering a round of units and their K and V (112 MB) exceed what L2
+    holds, so the schedule takes groups of 2 heads with a last group of 1;
+    sampled rows of a head in the first, a middle and the last group."""
+    mx, mean, n = _sampled_parity(1, 7, 32768, 128, seed=6, n_random=4, heads=(0, 3, 6),
+                                  causal=False)
+    print("unequal groups sampled rows %d: max %.3e mean %.3e" % (n, mx, mean))
+
+
 def test_deterministic():
     q, k, v = (t.cuda() for t in qkv_inputs.normal_qkv(1, 4, 1000, 1000, 128, 5,
                                                         dtype=torch.bfloat16))
