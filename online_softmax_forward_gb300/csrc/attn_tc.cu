@@ -33,10 +33,11 @@
 //    exponentiates the current ones; PV_t(j) follows once P_t(j) is written.
 //    A K/V stage is released when both issuers are done with it.
 //  * Warps 0-3 / 4-7 (softmax warpgroups, one per query tile; one thread per
-//    query row, 224 registers each via setmaxnreg) read S from TMEM in two
-//    64-key halves (at d = 128 the second load overlaps the first half's row
-//    max; at d = 64 both are in flight at once), apply the causal / tail
-//    mask, take the row max, exponentiate with
+//    query row, 224 registers each via setmaxnreg) read S from TMEM with the
+//    load-and-reduce form of sm_103a (tcgen05.ld.red with .max: two 64-column
+//    loads that also return their maximum, so a tile's row max costs no
+//    instructions; only a diagonal or tail tile masks keys and takes its max
+//    in software), exponentiate with
 //    ex2 (scores pre-multiplied by scale*log2 e, paired fp32 arithmetic), sum,
 //    and write P as 16-bit values: at d = 128 into a shared-memory tile in the
 //    MMA's 128-byte-swizzled layout, at d = 64 into tensor memory with two
@@ -271,10 +272,6 @@ struct Half {
     uint32_t a[32], b[32];
 };
 
-__device__ __forceinline__ void tmem_ld_half(uint32_t taddr, Half &h) {
-    ptx::tmem_ld32(taddr, h.a);
-    ptx::tmem_ld32(taddr + 32, h.b);
-}
 __device__ __forceinline__ void fence_half(Half &h) {
     reg_fence(h.a);
     reg_fence(h.b);
@@ -640,32 +637,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ptx::tc_fence_after();
                 const int kv0 = j * BN;
                 Half ra, rb;
-                float mxa;
-                if constexpr (D == 64) {
-                    // both halves in flight at once, in two 64-column loads: at
-                    // d = 64 the softmax alone sets the pace (3.5 % faster)
-                    ptx::tmem_ld64(tS, ra.a, ra.b);
-                    ptx::tmem_ld64(tS + 64, rb.a, rb.b);
-                    ptx::tmem_wait_ld();
-                    fence_half(ra);
-                    fence_half(rb);
-                    mask_half(ra, kv0, limit);
-                    mxa = max_half(ra);
-                } else {
-                    tmem_ld_half(tS, ra);
-                    ptx::tmem_wait_ld();
-                    fence_half(ra);
-                    tmem_ld_half(tS + 64, rb);  // in flight while the first half is reduced
-                    mask_half(ra, kv0, limit);
-                    mxa = max_half(ra);
-                    ptx::tmem_wait_ld();
-                    fence_half(rb);
-                }
+                // Both halves in flight at once.  The load-and-reduce form also
+                // returns each half's maximum, which is the row maximum of the
+                // tile unless some of its keys are masked.
+                float mxa, mxb;
+                ptx::tmem_ld64_max(tS, ra.a, ra.b, mxa);
+                ptx::tmem_ld64_max(tS + 64, rb.a, rb.b, mxb);
+                ptx::tmem_wait_ld();
+                fence_half(ra);
+                fence_half(rb);
+                asm volatile("" : "+f"(mxa), "+f"(mxb));  // read only after the wait
                 // S_t is in registers: the next S_t may be written
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(bars->s_free[t]));
-                mask_half(rb, kv0 + 64, limit);
-                const float smax = fmaxf(mxa, max_half(rb));  // raw maximum of the tile
+                float smax;  // raw maximum of the tile's visible keys
+                if (kv0 + BN > limit) {
+                    // diagonal or tail tile: masked keys must not set the maximum
+                    mask_half(ra, kv0, limit);
+                    mask_half(rb, kv0 + 64, limit);
+                    smax = fmaxf(max_half(ra), max_half(rb));
+                } else {
+                    smax = fmaxf(mxa, mxb);
+                }
                 const float m_new = fmaxf(m, smax * sl2);
                 bool rescale = false;
                 float alpha = 1.f;
