@@ -5,7 +5,7 @@
 // ("Online normalization"), in fp32, for small and latency-bound shapes and
 // for tile-size invariance tests.  Tile sizes are runtime values.
 //
-// Two kernels compute the same thing:
+// Three kernels compute the same thing:
 //
 // attn_f32_tiled_kernel (attn_fwd): fixed tiles of 32 query rows by 64 keys,
 // 128 threads, register-blocked.  Thread (ty, tx), ty in [0, 8), tx in
@@ -21,6 +21,13 @@
 // next V while the next scores are taken.  On grids with fewer blocks than
 // SMs, 2 or 4 warpgroups per block take the key tiles in turn and merge their
 // states at the end, each warpgroup finishing a quarter (or half) of the rows.
+//
+// attn_f32_keysplit_kernel (attn_fwd at d = 64 on grids of fewer than four
+// blocks per SM): 32 query rows per block, 8 warps; each warp walks every
+// eighth 32-key tile with its own online-softmax state for all 32 rows, in
+// 8 x 4 score and 8 x 8 output blocks per thread (12 float4 shared-memory
+// reads per 128 FMAs, against 8 per 64 above), and the warps' states are
+// combined at the end.
 //
 // attn_f32_kernel (attn_fwd_f32_blocked): runtime tile sizes, down to 1 x 1,
 // for the tile-size invariance tests.  One CTA owns one block of block_q
@@ -574,6 +581,254 @@ attn_f32_tiled_kernel(const float *__restrict__ q, const float *__restrict__ k,
     }
 }
 
+// ---------------------------------------------------------------- key-split kernel (d = 64)
+// 32 query rows per CTA, 8 warps; warp w takes the 32-key tiles w, w + 8, ...
+// of the block and keeps its own online-softmax state for all 32 rows, so one
+// thread owns an 8 x 4 block of scores (rows rg + 4i, keys kg + 8j; rg = lane
+// / 8, kg = lane % 8) and an 8 x 8 block of O (rows rg + 4i, columns
+// 4 kg + 32h + e).  Per head-dimension step of four, 12 float4 reads from
+// shared memory feed 128 FMAs (the 4 x 4 blocks of the tiled kernel: 8 per
+// 64), and every read instruction is one shared-memory wavefront.  P goes to
+// a per-warp transposed tile, so that the P V loop reads 8 rows' P with two
+// float4.  The row maximum and sum are reduced over the 8 lanes of a row
+// group with shuffles.  At the end the 8 warps' states are combined the way
+// partial softmax states combine (rescaled to the largest max).
+constexpr int kSW = 8;           // warps
+constexpr int kSQ = 32;          // query rows per CTA
+constexpr int kSK = 32;          // keys per warp tile
+constexpr int kSLd = 64 + 4;     // Q and K row stride: consecutive rows 4 banks apart
+constexpr int kSLdP = kSQ + 4;   // row stride of the transposed P tile
+constexpr int kSWarpFloats = kSK * kSLd + kSK * 64 + kSK * kSLdP;  // K, V, P^T of one warp
+constexpr int kSOffW = kSQ * kSLd;                                 // after Q
+constexpr size_t kSSmemBytes = sizeof(float) * (size_t)(kSOffW + kSW * kSWarpFloats);
+// the combination reuses the warps' areas: O [warp][row][64], then m, l [warp][row]
+static_assert(kSW * kSQ * 64 + 2 * kSW * kSQ <= kSW * kSWarpFloats, "state must fit");
+
+__global__ void __launch_bounds__(kSW * 32, 1)
+attn_f32_keysplit_kernel(const float *__restrict__ q, const float *__restrict__ k,
+                         const float *__restrict__ v, float *__restrict__ o,
+                         float *__restrict__ lse, int BH, int Sq, int Skv, int causal,
+                         float scale_log2, int nqb, int *status) {
+    constexpr int D = 64;
+    extern __shared__ __align__(16) float sm[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rg = lane >> 3, kg = lane & 7;
+    float *Qs = sm;
+    float *Kw = sm + kSOffW + warp * kSWarpFloats;  // [kSK][kSLd]
+    float *Vw = Kw + kSK * kSLd;                    // [kSK][64]
+    float *Pw = Vw + kSK * 64;                      // [kSK][kSLdP]: P^T, rows in the order rg*8 + i
+
+    const int64_t bh = blockIdx.x / nqb;
+    const int q0 = (blockIdx.x % nqb) * kSQ;
+    const int q_end = min(q0 + kSQ, Sq);
+    const int off = Skv - Sq;  // causal: key j visible to query i iff j <= i + off
+    if (!in_bounds(bh < BH, status)) return;  // block-uniform
+    const float *qg = q + (size_t)bh * Sq * D;
+    const float *kgp = k + (size_t)bh * Skv * D;
+    const float *vg = v + (size_t)bh * Skv * D;
+
+    int lim[8];  // keys visible to row rg + 4i: [0, lim[i])
+#pragma unroll
+    for (int i = 0; i < 8; ++i) lim[i] = causal ? min(Skv, q0 + rg + 4 * i + off + 1) : Skv;
+    const int kv_stop = causal ? min(Skv, q_end + off) : Skv;
+    const int ntiles = kv_stop > 0 ? (kv_stop + kSK - 1) / kSK : 0;
+    const int kv_all = causal ? min(Skv, q0 + off + 1) : Skv;  // visible to every row
+
+    float m[8], l[8], acc[8][2][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[i][h][e] = 0.f;
+    }
+
+    // Q by the whole block; this warp's first K and V as two more groups
+    stage_async<D>(Qs, kSLd, qg, q0, kSQ, Sq, threadIdx.x, kSW * 32, status);
+    cp_async_commit();
+    if (warp < ntiles) stage_async<D>(Kw, kSLd, kgp, warp * kSK, kSK, Skv, lane, 32, status);
+    cp_async_commit();
+    if (warp < ntiles) stage_async<D>(Vw, D, vg, warp * kSK, kSK, Skv, lane, 32, status);
+    cp_async_commit();
+    cp_async_wait1();  // Q and K have landed; V may still be arriving
+    __syncthreads();
+
+    for (int tile = warp; tile < ntiles; tile += kSW) {
+        const int kv0 = tile * kSK;
+        const bool more = tile + kSW < ntiles;
+        float s[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+#pragma unroll 2
+        for (int c = 0; c < D; c += 4) {
+            float4 qa[8], kb[4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                qa[i] = *reinterpret_cast<const float4 *>(Qs + (rg + 4 * i) * kSLd + c);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                kb[j] = *reinterpret_cast<const float4 *>(Kw + (kg + 8 * j) * kSLd + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float x = s[i][j];
+                    x = fmaf(qa[i].x, kb[j].x, x);
+                    x = fmaf(qa[i].y, kb[j].y, x);
+                    x = fmaf(qa[i].z, kb[j].z, x);
+                    x = fmaf(qa[i].w, kb[j].w, x);
+                    s[i][j] = x;
+                }
+        }
+        __syncwarp();  // every lane is done with K: the next K may load
+        if (more) stage_async<D>(Kw, kSLd, kgp, kv0 + kSW * kSK, kSK, Skv, lane, 32, status);
+        cp_async_commit();
+
+        // online softmax per row, as in the tiled kernel: max of the raw scores
+        // over the row group's 8 lanes, one FMA into log2 units, exp2
+        if (kv0 + kSK > kv_all) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (kv0 + kg + 8 * j >= lim[i]) s[i][j] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmax3(s[i][0], s[i][1], s[i][2]), s[i][3]);
+#pragma unroll
+        for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], w));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float m_new = fmaxf(m[i], mx[i] * scale_log2);
+            float alpha = 1.f, sum = 0.f;
+            if (m_new == -INFINITY) {  // no visible key yet: P = 0, nothing to rescale
+#pragma unroll
+                for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+            } else {
+                alpha = m[i] == -INFINITY ? 0.f : exp2f(m[i] - m_new);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    s[i][j] = exp2f(fmaf(s[i][j], scale_log2, -m_new));
+                    sum += s[i][j];
+                }
+            }
+            m[i] = m_new;
+            l[i] = l[i] * alpha + sum;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][h][e] *= alpha;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float *pr = Pw + (kg + 8 * j) * kSLdP + rg * 8;
+            *reinterpret_cast<float4 *>(pr) = make_float4(s[0][j], s[1][j], s[2][j], s[3][j]);
+            *reinterpret_cast<float4 *>(pr + 4) = make_float4(s[4][j], s[5][j], s[6][j], s[7][j]);
+        }
+        cp_async_wait1();  // this tile's V (the next K may still be arriving)
+        __syncwarp();      // P and V written by the other lanes are visible
+
+        // O += P V for rows rg + 4i, columns 4 kg + 32h + e
+#pragma unroll 4
+        for (int kk = 0; kk < kSK; ++kk) {
+            const float4 p0 = *reinterpret_cast<const float4 *>(Pw + kk * kSLdP + rg * 8);
+            const float4 p1 = *reinterpret_cast<const float4 *>(Pw + kk * kSLdP + rg * 8 + 4);
+            const float pr[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float4 vv = *reinterpret_cast<const float4 *>(Vw + kk * D + 4 * kg + 32 * h);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    acc[i][h][0] = fmaf(pr[i], vv.x, acc[i][h][0]);
+                    acc[i][h][1] = fmaf(pr[i], vv.y, acc[i][h][1]);
+                    acc[i][h][2] = fmaf(pr[i], vv.z, acc[i][h][2]);
+                    acc[i][h][3] = fmaf(pr[i], vv.w, acc[i][h][3]);
+                }
+            }
+        }
+        __syncwarp();  // every lane is done with V and P: the next V may load
+        if (more) stage_async<D>(Vw, D, vg, kv0 + kSW * kSK, kSK, Skv, lane, 32, status);
+        cp_async_commit();
+        cp_async_wait1();  // the next K (the next V may still be arriving)
+        __syncwarp();
+    }
+    cp_async_wait0();
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int w = 4; w > 0; w >>= 1) l[i] += __shfl_xor_sync(0xffffffffu, l[i], w);
+
+    // combine the 8 warps' states: each leaves (m, l, O) in the shared area
+    __syncthreads();  // every warp is done with its K, V and P
+    float *Os = sm + kSOffW;          // [warp][row][64]
+    float *Ms = Os + kSW * kSQ * 64;  // [warp][row]
+    float *Ls = Ms + kSW * kSQ;       // [warp][row]
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = rg + 4 * i;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            *reinterpret_cast<float4 *>(Os + (warp * kSQ + r) * 64 + 4 * kg + 32 * h) =
+                make_float4(acc[i][h][0], acc[i][h][1], acc[i][h][2], acc[i][h][3]);
+        if (kg == 0) {
+            Ms[warp * kSQ + r] = m[i];
+            Ls[warp * kSQ + r] = l[i];
+        }
+    }
+    __syncthreads();
+    // thread t finishes row t / 8, columns 8 (t % 8) .. + 7
+    const int r = threadIdx.x >> 3, c0 = (threadIdx.x & 7) * 8;
+    const int row = q0 + r;
+    if (row >= Sq) return;
+    if (!in_bounds(((size_t)bh * Sq + row) * D + c0 + 8 <= (size_t)BH * Sq * D, status)) return;
+    float mm = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kSW; ++w) mm = fmaxf(mm, Ms[w * kSQ + r]);
+    float ll = 0.f;
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kSW; ++w) {
+        const float mw = Ms[w * kSQ + r];
+        const float sc = mw == -INFINITY ? 0.f : exp2f(mw - mm);
+        ll = fmaf(Ls[w * kSQ + r], sc, ll);
+        const float4 x0 = *reinterpret_cast<const float4 *>(Os + (w * kSQ + r) * 64 + c0);
+        const float4 x1 = *reinterpret_cast<const float4 *>(Os + (w * kSQ + r) * 64 + c0 + 4);
+        a[0] = fmaf(x0.x, sc, a[0]); a[1] = fmaf(x0.y, sc, a[1]);
+        a[2] = fmaf(x0.z, sc, a[2]); a[3] = fmaf(x0.w, sc, a[3]);
+        a[4] = fmaf(x1.x, sc, a[4]); a[5] = fmaf(x1.y, sc, a[5]);
+        a[6] = fmaf(x1.z, sc, a[6]); a[7] = fmaf(x1.w, sc, a[7]);
+    }
+    const float inv = ll > 0.f ? 1.f / ll : 0.f;
+    float *orow = o + ((size_t)bh * Sq + row) * D + c0;
+    *reinterpret_cast<float4 *>(orow) = make_float4(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv);
+    *reinterpret_cast<float4 *>(orow + 4) = make_float4(a[4] * inv, a[5] * inv, a[6] * inv, a[7] * inv);
+    if (lse && c0 == 0)
+        lse[(size_t)bh * Sq + row] = ll > 0.f ? (mm + log2f(ll)) * 0.69314718055994530942f : -INFINITY;
+}
+
+int launch_keysplit(const float *q, const float *k, const float *v, float *o, float *lse,
+                    const Problem &p, cudaStream_t stream) {
+    const int nqb = (p.Sq + kSQ - 1) / kSQ;
+    const int64_t grid = p.bh() * nqb;
+    if (grid > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+    if (!set_smem_limit_once(reinterpret_cast<const void *>(attn_f32_keysplit_kernel),
+                             (int)kSSmemBytes))
+        return ATTN_ERR_LAUNCH;
+    int *status = status_word_device_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    attn_f32_keysplit_kernel<<<(unsigned)grid, kSW * 32, kSSmemBytes, stream>>>(
+        q, k, v, o, lse, (int)p.bh(), p.Sq, p.Skv, p.causal, p.scale * 1.4426950408889634f, nqb,
+        status);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
 template <int D, int KS, int NS>
 int launch_tiled_ks(const float *q, const float *k, const float *v, float *o, float *lse,
                     const Problem &p, int64_t grid, int nqb, cudaStream_t stream) {
@@ -628,6 +883,12 @@ int launch_tiled_d(const float *q, const float *k, const float *v, float *o, flo
     if (grid > INT32_MAX) return ATTN_ERR_INVALID_ARG;
     const int sms = device_sm_count();
     const int key_tiles = (p.Skv + kTK - 1) / kTK;  // of the block that sees the most keys
+    // d = 64 below four blocks per SM: the key-split kernel (B=2, H=4, S=512:
+    // 24.4 -> 22.5 us; B=1, H=8, S=2048 causal: +20 %); on larger grids the
+    // one-warpgroup blocks below are 3-4 % faster (B=2, H=40, S=1024)
+    if constexpr (D == 64) {
+        if (sms > 0 && grid < 4 * (int64_t)sms) return launch_keysplit(q, k, v, o, lse, p, stream);
+    }
     if constexpr (D <= 64) {
         if (sms > 0 && grid < sms && key_tiles > 1) {
             if constexpr (D >= 32) return launch_tiled_ks<D, 4, 1>(q, k, v, o, lse, p, grid, nqb, stream);

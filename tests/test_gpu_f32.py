@@ -153,3 +153,17 @@ def test_attn_fwd_tiled_kernel(d, bh, sq, skv, causal):
     o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
     o, lse = run(q, k, v, causal)
     assert_f32_parity(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("sq,skv", [(70, 2000), (1, 777), (33, 5), (300, 1200)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_d64_key_split_long_keys(sq, skv, causal):
+    """d = 64 runs on the key-split kernel (8 warps take the 32-key tiles of a
+    32-row block in turn, each with its own online softmax state, combined at
+    the end): keys long enough that every warp walks several tiles (2000 keys:
+    63 tiles), fewer keys than one tile, one query row, and causal rows that
+    see a prefix of the keys (Sq < Skv: the causal diagonal is offset)."""
+    q, k, v = f32(*qkv_inputs.normal_qkv(2, 3, sq, skv, 64, sq + skv))
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    o, lse = run(q, k, v, causal)
+    assert_f32_parity(o, lse, o_ref, lse_ref)
