@@ -3,7 +3,7 @@ ATTN_BOUNDS_CHECK) on the shapes that exercise the edges of the index
 arithmetic: ragged tails, Sq > Skv and Sq < Skv under the bottom-right
 causal mask, d = 64, 16-bit and fp32 outputs, every fp32 launch shape
 (one warpgroup with one or two stages, two and four warpgroups splitting
-the keys), runtime tiles of 7 and 13 x 19, split-KV with the warp-per-row
+the keys, the d = 64 key-split kernel), runtime tiles of 7 and 13 x 19, split-KV with the warp-per-row
 and the CTA-per-row merge, attn_merge and the no-alloc entry point.
 
 Each kernel tests every global-memory index and TMA coordinate it computes
@@ -91,9 +91,11 @@ F32_CASES = [
     (1, 1, 64, 64, 32, True),      # one key tile: one warpgroup
     (1, 1, 8, 1024, 32, False),    # few blocks, many key tiles: four warpgroups
     (2, 3, 77, 150, 16, True),     # d = 16: two warpgroups, two stages
-    (2, 4, 512, 512, 64, False),   # B=2, H=4, S=512: four warpgroups
+    (2, 4, 512, 512, 64, False),   # B=2, H=4, S=512, d = 64: the key-split kernel
     (4, 40, 300, 300, 128, True),  # many blocks: one warpgroup per block
-    (1, 3, 70, 40, 64, True),      # Sq > Skv
+    (1, 3, 70, 40, 64, True),      # Sq > Skv (key-split kernel)
+    (1, 2, 33, 2000, 64, True),    # key-split kernel, several tiles per warp, ragged rows
+    (4, 40, 300, 300, 64, True),   # d = 64 on a large grid: one warpgroup per block
 ]
 
 

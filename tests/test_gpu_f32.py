@@ -139,9 +139,11 @@ def test_attn_fwd_tiled_kernel(d, bh, sq, skv, causal):
     """attn_fwd's register-tiled kernel (32 query rows x 64 keys per tile).
     With fewer query blocks than SMs (B*H = 2) and more than one key tile,
     several warpgroups per block take the key tiles in turn and merge their
-    states (four with one K/V stage at d = 32 and 64, two with two stages at
+    states (four with one K/V stage at d = 32, two with two stages at
     d = 16); Skv = 300 and 130 give 5 and 3 key tiles, so some warpgroups get
-    one tile, one gets two, and with 3 tiles one gets none.  With one key tile
+    one tile, one gets two, and with 3 tiles one gets none.  At d = 64 grids
+    of fewer than four blocks per SM (all but B*H = 80 with 300 rows) run on
+    the key-split kernel instead (8 warps over 32-key tiles).  With one key tile
     (Skv = 37), with more blocks, and at d = 128, one warpgroup per block does
     it all, with two stages while the whole grid fits on the GPU at once and
     one stage beyond.  On 152 SMs: B*H = 40 with 130 rows (200 blocks) takes
