@@ -12,8 +12,8 @@
 //    consecutive 128-row query tiles (Q0, Q1) of one (batch, head) slice; they
 //    share every K/V tile.  Units are handed out dynamically: the producer
 //    of a CTA claims the next unit index from a device counter when it has
-//    issued the loads of the current one, and passes it to the CTA's other
-//    roles through a small ring in shared memory.  The order of the indices
+//    issued the loads of the current one, decodes it, and passes the decoded
+//    unit to the CTA's other roles through a small ring in shared memory.  The order of the indices
 //    (decode_unit) takes the (batch, head) slices in groups of about one
 //    round of units, longest first inside a group, so the CTAs running at
 //    any time share the K and V of a few heads through L2: each K/V tile is
@@ -119,6 +119,11 @@ struct Cfg {
 };
 constexpr int kMaxStages = 6;
 
+struct Unit {
+    int bh, q0;
+    int nkv[2];
+};
+
 struct Bars {
     uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
@@ -129,7 +134,7 @@ struct Bars {
     uint64_t o_empty[2];  // epilogue has read O_t (128 arrivals)
     uint64_t mma_done[2];
     uint64_t sched_full[kSchedRing], sched_empty[kSchedRing];
-    int sched_unit[kSchedRing];  // unit index, or -2: no more units
+    Unit sched_unit[kSchedRing];  // the decoded unit; bh = -2: no more units
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -148,11 +153,6 @@ struct TcParams {
     int out_f32;       // 1: o is fp32; 0: o has the input type
     int hook;
     unsigned long long timeout_ns;
-};
-
-struct Unit {
-    int bh, q0;
-    int nkv[2];
 };
 
 // Unit u of the schedule.  The (batch, head) slices are taken in groups of
@@ -401,11 +401,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // The next work unit for a consumer warp (issuer, softmax): the
     // producer's k-th claim, read from ring slot k mod kSchedRing and released
     // by one arrival per warp.  False if the CTA is aborting.
-    auto next_unit = [&](uint32_t &k, int &u) {
+    auto next_unit = [&](uint32_t &k, Unit &w) {
         const uint32_t s = k % kSchedRing;
         if (!__all_sync(0xffffffffu, watch.wait(bar(bars->sched_full[s]), (k / kSchedRing) & 1)))
             return false;
-        u = *reinterpret_cast<volatile int *>(&bars->sched_unit[s]);
+        const volatile Unit *su = &bars->sched_unit[s];
+        w.bh = su->bh;
+        w.q0 = su->q0;
+        w.nkv[0] = su->nkv[0];
+        w.nkv[1] = su->nkv[1];
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(bars->sched_empty[s]));
         ++k;
@@ -450,11 +454,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     ok = false;
                     break;
                 }
-                const int u = claim < (unsigned)p.n_units ? (int)claim : -2;
-                *reinterpret_cast<volatile int *>(&bars->sched_unit[slot]) = u;
+                // the unit is decoded once here and published whole, so that
+                // the other roles start it without integer divisions
+                Unit w{-2, 0, {0, 0}};
+                if (claim < (unsigned)p.n_units) w = decode_unit((int)claim, p);
+                volatile Unit *su = &bars->sched_unit[slot];
+                su->bh = w.bh;
+                su->q0 = w.q0;
+                su->nkv[0] = w.nkv[0];
+                su->nkv[1] = w.nkv[1];
                 ptx::mbar_arrive(bar(bars->sched_full[slot]));
-                if (u < 0) break;
-                const Unit w = decode_unit(u, p);
+                if (w.bh < 0) break;
                 const int nmax = max(w.nkv[0], w.nkv[1]);
                 if (nmax == 0) {
                     claim = atomicAdd(p.sched, 1u);
@@ -575,10 +585,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             return true;
         };
         for (uint32_t k = 0; ok;) {
-            int u;
-            if (!next_unit(k, u)) { ok = false; break; }
-            if (u < 0) break;
-            const Unit w = decode_unit(u, p);
+            Unit w;
+            if (!next_unit(k, w)) { ok = false; break; }
+            if (w.bh < 0) break;
             const int nmax = max(w.nkv[0], w.nkv[1]);
             const int my = w.nkv[t];
             if (nmax == 0) continue;
@@ -616,10 +625,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         bool ok = true;
 
         for (uint32_t k = 0; ok;) {
-            int u;
-            if (!next_unit(k, u)) { ok = false; break; }
-            if (u < 0) break;
-            const Unit w = decode_unit(u, p);
+            Unit w;
+            if (!next_unit(k, w)) { ok = false; break; }
+            if (w.bh < 0) break;
             const int nk = w.nkv[t];
             const int row = w.q0 + t * BM + r;  // query index of this thread
             const int limit = p.causal ? min(p.Skv, row + off + 1) : p.Skv;  // keys < limit visible
