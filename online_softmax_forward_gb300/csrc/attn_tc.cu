@@ -465,6 +465,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 su->nkv[1] = w.nkv[1];
                 ptx::mbar_arrive(bar(bars->sched_full[slot]));
                 if (w.bh < 0) break;
+                // The Q tiles of the new unit into L2 now.  Their loads below
+                // wait until the current unit's last S of that tile is computed,
+                // and Q is read only once, so they would otherwise start from
+                // HBM about one key tile before the softmax needs them.
+                for (int t = 0; t < 2; ++t)
+                    if (w.nkv[t] > 0 &&
+                        in_bounds(w.q0 + t * BM < p.Sq && w.bh >= 0 && w.bh < p.BH, p.status))
+                        for (int c = 0; c < C::kChunks; ++c)
+                            ptx::tma_prefetch_3d(&tm_q, c * 64, w.q0 + t * BM, w.bh);
                 const int nmax = max(w.nkv[0], w.nkv[1]);
                 if (nmax == 0) {
                     claim = atomicAdd(p.sched, 1u);
