@@ -118,31 +118,10 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives
-// lane (taddr.lane + t), columns taddr.col .. +31.
-// 64 consecutive columns of this warp's 32 lanes in one instruction: columns
-// taddr .. +31 into a, +32 .. +63 into b.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&a)[32], uint32_t (&b)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
-        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
-        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]),
-          "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]),
-          "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]),
-          "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]),
-          "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]),
-          "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]),
-          "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]),
-          "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]),
-          "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]),
-          "=r"(b[31])
-        : "r"(taddr));
-}
-// tmem_ld64 with the load-and-reduce form of sm_103a (tcgen05.ld.red, .max):
-// `mx` also receives the largest of the 64 fp32 values this thread loads.
+// 64 consecutive columns of this warp's 32 lanes in one instruction (columns
+// taddr .. +31 into a, +32 .. +63 into b), in the load-and-reduce form of
+// sm_103a (tcgen05.ld.red, .max): `mx` also receives the largest of the 64
+// fp32 values this thread loads.
 // Like the loaded registers, `mx` may be read only after tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_ld64_max(uint32_t taddr, uint32_t (&a)[32], uint32_t (&b)[32],
                                               float &mx) {
@@ -164,6 +143,8 @@ __device__ __forceinline__ void tmem_ld64_max(uint32_t taddr, uint32_t (&a)[32],
           "=r"(b[31]), "=f"(mx)
         : "r"(taddr));
 }
+// 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives
+// lane (taddr.lane + t), columns taddr.col .. +31.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
