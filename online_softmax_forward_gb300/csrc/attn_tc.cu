@@ -13,16 +13,17 @@
 //    share every K/V tile.  Units are handed out dynamically: the producer
 //    of a CTA claims the next unit index from a device counter when it has
 //    issued the loads of the current one, decodes it, and passes the decoded
-//    unit to the CTA's other roles through a small ring in shared memory.  The order of the indices
-//    (decode_unit) takes the (batch, head) slices in groups of about one
-//    round of units, longest first inside a group, so the CTAs running at
-//    any time share the K and V of a few heads through L2: each K/V tile is
-//    read from HBM about once.
+//    unit to the CTA's other roles through a small ring in shared memory.
+//    The order of the indices (decode_unit) takes the (batch, head) slices
+//    in groups of about one round of units, longest first inside a group, so
+//    the CTAs running at any time share the K and V of a few heads through
+//    L2: each K/V tile is read from HBM about once.
 //  * Warp 8 (producer) streams Q0/Q1 and the K/V tiles with TMA (128-byte
 //    swizzle) into a ring of shared-memory stages guarded by mbarriers, in
 //    the order the tensor core consumes them: K_0, then K_{j+1}, V_j for each
 //    j.  Each query tile has its own Q buffer and barriers, so the next unit's
-//    Q_t is fetched as soon as the last S_t of the current unit is computed.
+//    Q_t is fetched as soon as the last S_t of the current unit is computed;
+//    it is prefetched into L2 when the unit is published.
 //  * Warps 9 and 10 issue the tcgen05.mma (kind::f16, fp32 accumulate) of
 //    query tile 0 and 1 respectively, as whole warps with one elected lane:
 //        S_t = Q_t K_j^T  (shared-memory operands, fp32 result in TMEM)
@@ -37,20 +38,20 @@
 //    load-and-reduce form of sm_103a (tcgen05.ld.red with .max: two 64-column
 //    loads that also return their maximum, so a tile's row max costs no
 //    instructions; only a diagonal or tail tile masks keys and takes its max
-//    in software), exponentiate with
-//    ex2 (scores pre-multiplied by scale*log2 e, paired fp32 arithmetic), sum,
-//    and write P as 16-bit values: at d = 128 into a shared-memory tile in the
-//    MMA's 128-byte-swizzled layout, at d = 64 into tensor memory with two
-//    32-column stores (no swizzle, no proxy fence; 7-9 % faster).  The running max is updated lazily: O and l are
-//    rescaled (O in TMEM, after the previous P.V has completed) only when the
-//    max grows by more than 2^8, so P stays <= 256; O, l and m always refer
-//    to the same stale max, so the result is the same softmax.  Each row
-//    keeps two normalisers: l, the sum of the exact P, gives the lse; lr
-//    adds to it, tile by tile, the rounding error of the tile's largest P in
-//    its 16-bit form -- the term a stale max makes large (up to 256 * 2^-9)
-//    -- so that O / lr divides by (almost exactly) the sum of the weights
-//    P.V multiplied.  After the last tile they write O / lr and
-//    lse = m + ln l.
+//    in software), exponentiate with ex2 (scores pre-multiplied by
+//    scale*log2 e, paired fp32 arithmetic), sum, and write P as 16-bit
+//    values: at d = 128 into a shared-memory tile in the MMA's
+//    128-byte-swizzled layout, at d = 64 into tensor memory with two
+//    32-column stores (no swizzle, no proxy fence; 7-9 % faster).  The
+//    running max is updated lazily: O and l are rescaled (O in TMEM, after
+//    the previous P.V has completed) only when the max grows by more than
+//    2^8, so P stays <= 256; O, l and m always refer to the same stale max,
+//    so the result is the same softmax.  Each row keeps two normalisers: l,
+//    the sum of the exact P, gives the lse; lr adds to it, tile by tile, the
+//    rounding error of the tile's largest P in its 16-bit form -- the term a
+//    stale max makes large (up to 256 * 2^-9) -- so that O / lr divides by
+//    (almost exactly) the sum of the weights P.V multiplied.  After the last
+//    tile they write O / lr and lse = m + ln l.
 //  * Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0, O1 after;
 //    at d = 64 also P0 [384,448) and P1 [448,512), 16-bit pairs per column.
 //  * Every mbarrier wait is bounded (globaltimer).  On expiry the CTA sets an
