@@ -93,6 +93,39 @@ def test_rising_maximum_forces_rescale():
         assert_bf16_parity(o, lse, o_ref, lse_ref)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_masked_keys_never_set_the_row_max(d, dtype):
+    """The softmax takes a tile's row maximum from the TMEM load itself, which
+    covers all 128 keys of the tile; on a diagonal or tail tile some of them
+    are masked and must not count.  Two inputs make any masked key that did
+    count push the running maximum so far above the visible scores that
+    their probabilities flush to zero:
+    * causal, 256 keys, keys 192-255 scoring ~300 above the rest: rows 128-191
+      see the first 64 keys of the diagonal tile only, next to masked keys
+      300 higher;
+    * non-causal, 200 keys all scoring about -300: the 56 key slots past the
+      end of the tail tile load as zeros, i.e. score 0, 300 above every
+      visible key.
+    Both must match the oracle at the standard bounds."""
+    scale = 1.0 / math.sqrt(d)
+    g = torch.Generator().manual_seed(33)
+    cases = []
+    q = torch.ones(1, 2, 256, d)
+    k = 0.05 * torch.randn(1, 2, 256, d, generator=g)
+    k[:, :, 192:] += 300.0 / (scale * d)
+    cases.append((q, k, torch.randn(1, 2, 256, d, generator=g), True))
+    q = torch.ones(1, 2, 130, d)
+    k = -300.0 / (scale * d) + 0.05 * torch.randn(1, 2, 200, d, generator=g)
+    cases.append((q, k, torch.randn(1, 2, 200, d, generator=g), False))
+    for q, k, v, causal in cases:
+        q, k, v = q.to(dtype), k.to(dtype), v.to(dtype)
+        o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+        o, lse = run(q, k, v, causal, dtype=dtype, out_dtype=torch.float32)
+        assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+        assert_bf16_parity(o, lse, o_ref, lse_ref)
+
+
 def _sampled_parity(B, H, S, d, seed, n_random, heads=None, rows_per_head=None, causal=True,
                     dtype=torch.bfloat16):
     ensure_built()
