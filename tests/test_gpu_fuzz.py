@@ -1,7 +1,7 @@
 """Seeded random shapes through every path, each compared element by element
 with the fp64 oracle.  The shapes are drawn once from a fixed seed, so the
 cases are the same on every run: B, H in 1..3, Sq and Skv in 1..700 (ragged
-against every tile size the kernels use), causal or not, every supported
+against every tile size the kernels use) and, for ten more, in 1..3000, causal or not, every supported
 head width and input type, fp32 or 16-bit output, attn_fwd and split-KV with
 a random split count."""
 import random
@@ -18,21 +18,23 @@ from gpu_util import (assert_bf16_parity, assert_f32_parity, assert_lse_close,
 pytestmark = pytest.mark.gpu
 
 
-def _cases(n, seed):
+def _cases(n, seed, max_len=700, first=0):
     rng = random.Random(seed)
     out = []
     for i in range(n):
         dt = rng.choice([torch.float32, torch.bfloat16, torch.float16])
         d = rng.choice([16, 32, 64, 128] if dt == torch.float32 else [64, 128])
         out.append(dict(
-            B=rng.randint(1, 3), H=rng.randint(1, 3), Sq=rng.randint(1, 700),
-            Skv=rng.randint(1, 700), d=d, causal=rng.random() < 0.5, dtype=dt,
+            B=rng.randint(1, 3), H=rng.randint(1, 3), Sq=rng.randint(1, max_len),
+            Skv=rng.randint(1, max_len), d=d, causal=rng.random() < 0.5, dtype=dt,
             out32=dt == torch.float32 or rng.random() < 0.5,
-            splitkv=rng.random() < 0.3, n_splits=rng.randint(1, 12), seed=1000 + i))
+            splitkv=rng.random() < 0.3, n_splits=rng.randint(1, 12), seed=1000 + first + i))
     return out
 
 
-CASES = _cases(24, 20261203)
+# short sequences (every tile size, ragged), then longer ones (several units per
+# head on the tensor-core kernel, several key tiles per warp on the fp32 kernels)
+CASES = _cases(24, 20261203) + _cases(10, 7, max_len=3000, first=100)
 
 
 def _id(c):
