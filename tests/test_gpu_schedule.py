@@ -118,3 +118,25 @@ def test_concurrent_host_threads():
     for i in range(n_threads):
         for o, lse, of in outs[i]:
             assert torch.equal(o, ref_o) and torch.equal(lse, ref_l) and torch.equal(of, ref_f)
+
+
+def test_full_size_launches_identical():
+    """B=1, H=32, S=8192, d=128 causal (1,024 units over the persistent grid,
+    several claims per CTA): 40 launches, each into an output pre-filled with
+    NaN, must each equal the first launch bit for bit -- the units a CTA
+    claims differ from launch to launch, the result may not."""
+    ensure_built()
+    q, k, v = (t.cuda() for t in qkv_inputs.normal_qkv(1, 32, 8192, 8192, 128, seed=52,
+                                                       dtype=torch.bfloat16))
+    ref_o, ref_l = pkg.attention(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    o, lse = torch.empty_like(ref_o), torch.empty_like(ref_l)
+    bad = 0
+    for _ in range(40):
+        o.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        pkg.attention(q, k, v, causal=True, out=o, lse=lse)
+        bad += int(not (torch.equal(o, ref_o) and torch.equal(lse, ref_l)))
+    torch.cuda.synchronize()
+    assert pkg.attn_check_status(None) == pkg.ATTN_OK
+    assert bad == 0
