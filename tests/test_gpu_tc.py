@@ -126,6 +126,26 @@ def test_masked_keys_never_set_the_row_max(d, dtype):
         assert_bf16_parity(o, lse, o_ref, lse_ref)
 
 
+@pytest.mark.parametrize("skv", [8192, 8193])
+@pytest.mark.parametrize("out32", [False, True])
+def test_output_store_paths_at_the_key_threshold(skv, out32):
+    """With up to 8192 keys (d = 128) the unit epilogue writes O through shared
+    memory, two rows or half rows per store instruction; with more keys it
+    stores each row directly.  Both paths, with 16-bit and fp32 output, on
+    ragged query rows (300 = 2 x 128 + 44) and 4 heads."""
+    q, k, v = qkv_inputs.normal_qkv(1, 4, 300, skv, 128, seed=skv + 3 * out32)
+    q, k, v = q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+    for causal in (False, True):
+        o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+        if out32:
+            o, lse = run(q, k, v, causal, dtype=torch.bfloat16, out_dtype=torch.float32)
+            assert_bf16_parity(o, lse, o_ref, lse_ref)
+        else:
+            o, lse = run(q, k, v, causal, dtype=torch.bfloat16, out_dtype=torch.bfloat16)
+            assert_rounded_output(o, o_ref, torch.bfloat16)
+            assert_lse_close(lse, lse_ref, 1e-4)
+
+
 def _sampled_parity(B, H, S, d, seed, n_random, heads=None, rows_per_head=None, causal=True,
                     dtype=torch.bfloat16):
     ensure_built()
